@@ -1,0 +1,24 @@
+"""Shared pytest configuration.
+
+Markers: ``gpu`` -- needs a GB300 (sm_103) and the CUDA library; everything
+else runs on the CPU.  The oracle is built on first use.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a GB300 GPU and the CUDA library")
+
+
+@pytest.fixture(scope="session")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
