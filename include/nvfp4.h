@@ -1,0 +1,221 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4.so: NVFP4 quantisers and block-scaled GEMMs
+ * for one GB300 (sm_103a), the hot path of an NVFP4 linear / MLP layer.
+ *
+ * The method is the NVFP4 pretraining recipe of the "NVFP4 pretraining
+ * recipe" page (re-post of NVIDIA's blog on NVFP4 in TransformerEngine and
+ * MaxText).  Each entry point below cites the passage of that page that
+ * defines what it computes.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named "device" are CUDA device pointers on the current device;
+ *    host pointers are marked "host".  The caller owns every buffer, including
+ *    workspaces and the per-tensor scalars; the library never allocates,
+ *    frees or synchronises on the hot path (nvfp4_check_device_errors is the
+ *    one call that synchronises).
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).
+ *  - Argument errors are reported by the return value before anything is
+ *    launched; a failed launch returns NVFP4_ERR_CUDA.  Device-side wait
+ *    timeouts (a hung pipeline) are recorded in a device error word and
+ *    reported by nvfp4_check_device_errors.
+ *  - Matrices are row-major.  A "K-major" NVFP4 operand [rows, K] stores the
+ *    E2M1 codes of row r in bytes r*K/2 .. r*K/2 + K/2 - 1, element 2i in the
+ *    low nibble and element 2i+1 in the high nibble.
+ *  - Scale tensors (E4M3, one byte per 16 elements) are stored in the layout
+ *    the block-scaled MMA reads: 512-byte atoms of 128 rows x 4 scale
+ *    columns, the byte of (row r, scale column c) at
+ *        atom(r/128, c/4) * 512 + (r%32)*16 + ((r/32)%4)*4 + c%4,
+ *    atoms row-block major, rows padded to 128 and scale columns to 4 with
+ *    zero bytes.  Size: pad128(rows) * pad4(cols/16) bytes.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* nvfp4_stream; /* a cudaStream_t */
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,    /* null pointer, bad enum or flag combination   */
+  NVFP4_ERR_SHAPE = 2,          /* a dimension breaks the rules stated per call */
+  NVFP4_ERR_ALIGN = 3,          /* a pointer or leading dimension is misaligned */
+  NVFP4_ERR_ARCH = 4,           /* the current device is not sm_103             */
+  NVFP4_ERR_WORKSPACE = 5,      /* workspace missing or smaller than required   */
+  NVFP4_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed            */
+  NVFP4_ERR_DEVICE_TIMEOUT = 7  /* a kernel's bounded wait expired              */
+} nvfp4_status;
+
+typedef enum { NVFP4_IN_BF16 = 0, NVFP4_IN_FP32 = 1 } nvfp4_in_dtype;
+
+/* Quantisation geometry ("NVFP4 pretraining recipe", bullets 1 and 4).
+ *  ROW_1X16   : 1x16 blocks along the contiguous dim; output [rows, cols].
+ *  COL_1X16   : 1x16 blocks along the rows; output is the transpose
+ *               [cols, rows] (K-major along the original rows), the form the
+ *               WGRAD GEMM consumes.
+ *  BLOCK_16X16: one scale per 16x16 tile (weights); output [rows, cols], and
+ *               with NVFP4_EMIT_T also the transpose [cols, rows] built from
+ *               the same codes (no requantisation). */
+typedef enum { NVFP4_ROW_1X16 = 0, NVFP4_COL_1X16 = 1, NVFP4_BLOCK_16X16 = 2 } nvfp4_mode;
+
+enum {
+  NVFP4_RHT = 1u,        /* 16-point random Hadamard transform along the blocks (bullet 3) */
+  NVFP4_SR = 2u,         /* stochastic rounding of the elements (bullet 5); else RNE       */
+  NVFP4_EMIT_T = 4u,     /* BLOCK_16X16 only: also write the transposed operand            */
+  NVFP4_AMAX_GIVEN = 8u  /* use *out->amax (device, set by the caller) as the tensor amax   */
+};
+
+/* A quantised NVFP4 operand.  The caller fills the pointers; nvfp4_quantize
+ * fills rows/cols/mode/flags.  rows x cols is the logical K-major operand
+ * (cols = contraction length).
+ *   codes    device uint8 [rows][cols/2]
+ *   scales   device uint8, MMA layout for [rows, cols]
+ *   codes_t  device uint8 [cols][rows/2]     (BLOCK_16X16 + EMIT_T, else NULL)
+ *   scales_t device uint8, MMA layout for [cols, rows] (likewise)
+ *   amax     device float: tensor amax (output; input with AMAX_GIVEN)
+ *   s_dec    device float: per-tensor decode scale 1/s_enc (output)        */
+typedef struct nvfp4_tensor {
+  void* codes;
+  void* scales;
+  void* codes_t;
+  void* scales_t;
+  float* amax;
+  float* s_dec;
+  int64_t rows;
+  int64_t cols;
+  int32_t mode;
+  uint32_t flags;
+} nvfp4_tensor;
+
+/* ---------------------------------------------------------------------- */
+/* Status and device                                                       */
+/* ---------------------------------------------------------------------- */
+const char* nvfp4_status_string(nvfp4_status s);
+/* Library version as major*10000 + minor*100 + patch. */
+int nvfp4_version(void);
+/* NVFP4_OK when `device` is an sm_103 GPU this library's kernels run on. */
+nvfp4_status nvfp4_device_check(int device);
+/* Synchronises `stream`, then reads and clears the device error word that
+ * kernels set when a bounded wait expires.  Returns NVFP4_ERR_DEVICE_TIMEOUT
+ * if it was set, NVFP4_ERR_CUDA if the stream reported an error. */
+nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream);
+
+/* ---------------------------------------------------------------------- */
+/* Quantiser                                                               */
+/* ---------------------------------------------------------------------- */
+/* Byte sizes for quantising an input x [rows, cols]: the codes (and, with
+ * EMIT_T, the same again for codes_t), the MMA-layout scales (scales_t has
+ * the size of the transposed operand's scales), and the workspace
+ * nvfp4_quantize needs.  Any output pointer may be NULL. */
+nvfp4_status nvfp4_quantize_sizes(int64_t rows, int64_t cols, int32_t mode, uint32_t flags,
+                                  size_t* codes_bytes, size_t* scales_bytes,
+                                  size_t* scales_t_bytes, size_t* workspace_bytes);
+
+/* NVFP4 quantisation of x [rows, cols] (row-major, leading dim ld elements),
+ * per "NVFP4 pretraining recipe", bullets 1-5:
+ *   amax_T = max |v| over the (RHT-transformed, if NVFP4_RHT) operand v;
+ *   s_enc = 6*448 / amax_T (1 if amax_T == 0, FLT_MAX if not finite),
+ *   s_dec = 1 / s_enc;
+ *   per block b (16 elements, or a 16x16 tile): a_b = max |v|,
+ *   S_b = E4M3_rn_satfinite((a_b / 6) * s_enc);
+ *   per element: y = v * (S_b == 0 ? 0 : s_enc / S_b), encoded to E2M1 by
+ *   round-to-nearest-even with saturation to +-6, or with NVFP4_SR by
+ *   stochastic rounding: round |y| up to the next grid value iff
+ *   r < floor(frac * 2^32), frac = (|y| - lo) / (hi - lo), where r is word
+ *   idx%4 of Philox4x32-10(key = seed, counter = (idx/4 lo, idx/4 hi, 0,
+ *   offset lo)) and idx = row*cols + col in the output layout.
+ *   NVFP4_RHT (1x16 modes): each block becomes (1/4) H16 diag(s) v, signs s_i
+ *   = -1 where bit i of word 0 of Philox(key = seed, counter = (0,0,1,0)) is
+ *   set -- one sign vector per seed, so both WGRAD operands quantised with the
+ *   same seed share it (bullet 3: RHT on the WGRAD inputs only).
+ * Shapes: ROW_1X16 needs cols % 16 == 0; COL_1X16 rows % 16 == 0 and
+ * cols % 8 == 0; BLOCK_16X16 rows % 16 == 0, cols % 16 == 0, no NVFP4_RHT.
+ * x must be 16-byte aligned and ld * element size a multiple of 16 bytes.
+ * The workspace (device, >= the size nvfp4_quantize_sizes gives, 16-byte
+ * aligned) holds per-CTA partial maxima; with NVFP4_AMAX_GIVEN it may be NULL.
+ * Outputs: out->codes/scales (+ codes_t/scales_t), out->amax, out->s_dec;
+ * padding bytes of the scale tensors are written as zero. */
+nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                            int64_t ld, int32_t mode, uint32_t flags, uint64_t seed,
+                            uint64_t offset, nvfp4_tensor* out, void* workspace,
+                            size_t workspace_bytes, nvfp4_stream stream);
+
+/* ---------------------------------------------------------------------- */
+/* Block-scaled GEMM                                                       */
+/* ---------------------------------------------------------------------- */
+/* Output modes of nvfp4_gemm. */
+enum {
+  NVFP4_D_BF16 = 0,        /* D bf16 [M,N] = bf16(alpha * acc)                            */
+  NVFP4_D_F32_ACCUM = 1,   /* D fp32 [M,N] += float(bf16(alpha * acc)) (master gradient)   */
+  NVFP4_D_BF16_ADD_C = 2   /* D bf16 [M,N] = bf16(alpha * acc + float(C)), C bf16 [M,N]    */
+};
+
+/* D = alpha * A . B^T with A [M, K] and B [N, K] NVFP4 K-major operands and
+ * alpha = (*A->s_dec) * (*B->s_dec) read on the device; FP32 accumulation in
+ * tensor memory, BF16 output ("NVFP4 pretraining recipe", Figure 1 text:
+ * FPROP, DGRAD and WGRAD consume NVFP4 inputs and emit BF16 outputs, later
+ * folded into the FP32 master weight -- NVFP4_D_F32_ACCUM).
+ * a_view / b_view: 0 reads codes/scales, 1 reads codes_t/scales_t (the
+ * transpose written by BLOCK_16X16 + EMIT_T: DGRAD reads W this way, bullet 4).
+ * The operand's logical shape must match (rows, cols) = (M, K) / (N, K).
+ * Shapes: M, N >= 1, K % 64 == 0, N % 8 == 0.  D (and C) 16-byte aligned.
+ * workspace: unused (may be NULL). */
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                        int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                        int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                        nvfp4_stream stream);
+
+/* As nvfp4_gemm with an explicit output tile width: tile_n = 128 or 256
+ * (0 picks the default).  For tuning and tests. */
+nvfp4_status nvfp4_gemm_ex(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                           int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                           int64_t N, int64_t K, int32_t tile_n, nvfp4_stream stream);
+
+/* ---------------------------------------------------------------------- */
+/* SwiGLU MLP (gate, up, down projections) with NVFP4 GEMMs                */
+/* ---------------------------------------------------------------------- */
+/* "NVFP4 pretraining recipe", Figure 1 text: the MLP's GEMMs run in NVFP4.
+ * Forward: G = X Wg^T, U = X Wu^T, H = silu(G) * U, Y = H Wd^T; backward:
+ * dH = dY Wd, dWd += dY^T H, dG/dU from the SwiGLU derivative, dX = dG Wg +
+ * dU Wu, dWg += dG^T X, dWu += dU^T X.  Quantisation per operand: X, H and W
+ * with RNE (1x16 / 16x16), dY, dG, dU with SR; the WGRAD operands (X^T, H^T,
+ * dY^T, dG^T, dU^T) COL_1X16 with the RHT when flags has NVFP4_RHT.
+ * Dimensions: M tokens, D hidden, F ffn; Wg, Wu fp32 [F, D], Wd fp32 [D, F]
+ * (device, the FP32 master weights, quantised 16x16 every forward). */
+typedef struct nvfp4_mlp_params {
+  int64_t M, D, F;
+  const float* Wg;
+  const float* Wu;
+  const float* Wd;
+  uint64_t seed;   /* RHT signs and SR key                           */
+  uint64_t step;   /* SR counter offsets 8*step + 0..5 (per tensor)  */
+  uint32_t flags;  /* NVFP4_RHT or 0                                 */
+} nvfp4_mlp_params;
+
+/* Device bytes of the saved-activation buffer (forward -> backward) and of
+ * the workspace either call needs. */
+nvfp4_status nvfp4_mlp_sizes(int64_t M, int64_t D, int64_t F, size_t* saved_bytes,
+                             size_t* workspace_bytes);
+
+/* X bf16 [M, D] -> Y bf16 [M, D]; fills `saved` (device) for the backward.
+ * Shapes: M, D, F multiples of 128. */
+nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, void* saved,
+                           size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                           nvfp4_stream stream);
+
+/* dY bf16 [M, D] -> dX bf16 [M, D]; dWg, dWu fp32 [F, D] and dWd fp32 [D, F]
+ * (device) are accumulated: += float(bf16(WGRAD)). */
+nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void* saved,
+                           void* dX, float* dWg, float* dWu, float* dWd, void* workspace,
+                           size_t workspace_bytes, nvfp4_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H */

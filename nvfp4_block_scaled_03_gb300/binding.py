@@ -1,0 +1,232 @@
+"""ctypes binding of libnvfp4.so with the C ABI's names (include/nvfp4.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  If the library is not
+built, importing this module raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass, field
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libnvfp4.so")
+
+# status codes
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_ARCH, ERR_WORKSPACE, ERR_CUDA, \
+    ERR_DEVICE_TIMEOUT = range(8)
+# enums and flags
+IN_BF16, IN_FP32 = 0, 1
+ROW_1X16, COL_1X16, BLOCK_16X16 = 0, 1, 2
+RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
+D_BF16, D_F32_ACCUM, D_BF16_ADD_C = 0, 1, 2
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class Tensor(C.Structure):
+    """Mirror of ``nvfp4_tensor``."""
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("codes_t", C.c_void_p),
+                ("scales_t", C.c_void_p), ("amax", C.c_void_p), ("s_dec", C.c_void_p),
+                ("rows", C.c_int64), ("cols", C.c_int64), ("mode", C.c_int32),
+                ("flags", C.c_uint32)]
+
+
+class MlpParams(C.Structure):
+    """Mirror of ``nvfp4_mlp_params``."""
+    _fields_ = [("M", C.c_int64), ("D", C.c_int64), ("F", C.c_int64), ("Wg", C.c_void_p),
+                ("Wu", C.c_void_p), ("Wd", C.c_void_p), ("seed", C.c_uint64),
+                ("step", C.c_uint64), ("flags", C.c_uint32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = C.CDLL(LIB_PATH)
+    i32, i64, u32, u64, vp, sz = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64, C.c_void_p, C.c_size_t
+    P = C.POINTER
+    sigs = {
+        "nvfp4_status_string": ([C.c_int], C.c_char_p),
+        "nvfp4_version": ([], C.c_int),
+        "nvfp4_device_check": ([C.c_int], C.c_int),
+        "nvfp4_check_device_errors": ([vp], C.c_int),
+        "nvfp4_quantize_sizes": ([i64, i64, i32, u32, P(sz), P(sz), P(sz), P(sz)], C.c_int),
+        "nvfp4_quantize": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp, sz, vp],
+                           C.c_int),
+        "nvfp4_gemm": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, vp, sz, vp],
+                       C.c_int),
+        "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
+                          C.c_int),
+        "nvfp4_mlp_sizes": ([i64, i64, i64, P(sz), P(sz)], C.c_int),
+        "nvfp4_mlp_fwd": ([P(MlpParams), vp, vp, vp, sz, vp, sz, vp], C.c_int),
+        "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+lib = _load()
+
+
+def status_string(s: int) -> str:
+    return lib.nvfp4_status_string(s).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise NVFP4Error(status, where)
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+@dataclass
+class QTensor:
+    """A quantised operand: the device buffers plus the ABI descriptor."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    amax: torch.Tensor
+    s_dec: torch.Tensor
+    codes_t: torch.Tensor | None = None
+    scales_t: torch.Tensor | None = None
+    desc: Tensor = field(default_factory=Tensor)
+
+    @property
+    def rows(self):
+        return self.desc.rows
+
+    @property
+    def cols(self):
+        return self.desc.cols
+
+
+def quantize_sizes(rows, cols, mode, flags=0):
+    c, s, st, w = C.c_size_t(), C.c_size_t(), C.c_size_t(), C.c_size_t()
+    _check(lib.nvfp4_quantize_sizes(rows, cols, mode, flags, C.byref(c), C.byref(s), C.byref(st),
+                                    C.byref(w)), "nvfp4_quantize_sizes")
+    return c.value, s.value, st.value, w.value
+
+
+def alloc_qtensor(rows, cols, mode, flags=0, device="cuda") -> QTensor:
+    """Allocate the output buffers of quantising an input [rows, cols]."""
+    cb, sb, stb, _ = quantize_sizes(rows, cols, mode, flags)
+    u8 = dict(dtype=torch.uint8, device=device)
+    q = QTensor(codes=torch.empty(cb, **u8), scales=torch.empty(sb, **u8),
+                amax=torch.zeros(1, dtype=torch.float32, device=device),
+                s_dec=torch.zeros(1, dtype=torch.float32, device=device))
+    if flags & EMIT_T:
+        q.codes_t = torch.empty(cb, **u8)
+        q.scales_t = torch.empty(stb, **u8)
+    d = q.desc
+    d.codes, d.scales = q.codes.data_ptr(), q.scales.data_ptr()
+    d.codes_t, d.scales_t = _ptr(q.codes_t), _ptr(q.scales_t)
+    d.amax, d.s_dec = q.amax.data_ptr(), q.s_dec.data_ptr()
+    return q
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes, device):
+    key = (str(device), torch.cuda.current_stream().cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def nvfp4_quantize(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0, offset: int = 0,
+                   out: QTensor | None = None, workspace: torch.Tensor | None = None,
+                   amax: float | torch.Tensor | None = None, stream=None) -> QTensor:
+    """Quantise a 2-D bf16/fp32 CUDA tensor (see nvfp4_quantize in nvfp4.h)."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    if x.dtype == torch.bfloat16:
+        dt = IN_BF16
+    elif x.dtype == torch.float32:
+        dt = IN_FP32
+    else:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    rows, cols = x.shape
+    if amax is not None:
+        flags |= AMAX_GIVEN
+    if out is None:
+        out = alloc_qtensor(rows, cols, mode, flags, device=x.device)
+    if amax is not None:
+        out.amax.copy_(torch.as_tensor(amax, dtype=torch.float32).reshape(1))
+    _, _, _, wsb = quantize_sizes(rows, cols, mode, flags)
+    if workspace is None and wsb:
+        workspace = _workspace(wsb, x.device)
+    _check(lib.nvfp4_quantize(x.data_ptr(), dt, rows, cols, x.stride(0), mode, flags, seed, offset,
+                              C.byref(out.desc), _ptr(workspace),
+                              0 if workspace is None else workspace.numel(), _stream(stream)),
+           "nvfp4_quantize")
+    return out
+
+
+def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,
+               out: torch.Tensor | None = None, d_mode: int = D_BF16,
+               C_add: torch.Tensor | None = None, tile_n: int = 0, stream=None) -> torch.Tensor:
+    """D = alpha * A . B^T (see nvfp4_gemm in nvfp4.h); returns D."""
+    M = A.desc.cols if a_view else A.desc.rows
+    K = A.desc.rows if a_view else A.desc.cols
+    N = B.desc.cols if b_view else B.desc.rows
+    if out is None:
+        dtype = torch.float32 if d_mode == D_F32_ACCUM else torch.bfloat16
+        out = (torch.zeros if d_mode == D_F32_ACCUM else torch.empty)(
+            (M, N), dtype=dtype, device=A.codes.device)
+    if tile_n:
+        st = lib.nvfp4_gemm_ex(C.byref(A.desc), a_view, C.byref(B.desc), b_view, out.data_ptr(),
+                               d_mode, _ptr(C_add), M, N, K, tile_n, _stream(stream))
+    else:
+        st = lib.nvfp4_gemm(C.byref(A.desc), a_view, C.byref(B.desc), b_view, out.data_ptr(),
+                            d_mode, _ptr(C_add), M, N, K, None, 0, _stream(stream))
+    _check(st, "nvfp4_gemm")
+    return out
+
+
+def mlp_sizes(M, D, F):
+    s, w = C.c_size_t(), C.c_size_t()
+    _check(lib.nvfp4_mlp_sizes(M, D, F, C.byref(s), C.byref(w)), "nvfp4_mlp_sizes")
+    return s.value, w.value
+
+
+def mlp_params(M, D, F, Wg, Wu, Wd, seed=0, step=0, rht=True) -> MlpParams:
+    return MlpParams(M, D, F, Wg.data_ptr(), Wu.data_ptr(), Wd.data_ptr(), seed, step,
+                     RHT if rht else 0)
+
+
+def nvfp4_mlp_fwd(p: MlpParams, X, Y, saved, workspace, stream=None):
+    _check(lib.nvfp4_mlp_fwd(C.byref(p), X.data_ptr(), Y.data_ptr(), saved.data_ptr(),
+                             saved.numel(), workspace.data_ptr(), workspace.numel(),
+                             _stream(stream)), "nvfp4_mlp_fwd")
+    return Y
+
+
+def nvfp4_mlp_bwd(p: MlpParams, dY, saved, dX, dWg, dWu, dWd, workspace, stream=None):
+    _check(lib.nvfp4_mlp_bwd(C.byref(p), dY.data_ptr(), saved.data_ptr(), dX.data_ptr(),
+                             dWg.data_ptr(), dWu.data_ptr(), dWd.data_ptr(), workspace.data_ptr(),
+                             workspace.numel(), _stream(stream)), "nvfp4_mlp_bwd")
+    return dX
+
+
+def check_device_errors(stream=None):
+    _check(lib.nvfp4_check_device_errors(_stream(stream)), "nvfp4_check_device_errors")

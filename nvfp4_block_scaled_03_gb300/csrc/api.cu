@@ -1,0 +1,114 @@
+// api.cu -- the extern "C" entry points of libnvfp4.so (declared and
+// documented in include/nvfp4.h): argument checks, device checks and
+// dispatch to the kernels' host launchers.
+#include <mutex>
+
+#include "internal.h"
+
+namespace nvfp4 {
+
+nvfp4_status current_device(DeviceInfo* info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 64) return NVFP4_ERR_CUDA;
+  if (!have[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = cache[dev];
+  if (info->major != 10 || info->minor != 3) return NVFP4_ERR_ARCH;
+  return NVFP4_OK;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_SHAPE: return "unsupported shape";
+    case NVFP4_ERR_ALIGN: return "misaligned pointer or leading dimension";
+    case NVFP4_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    case NVFP4_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+  }
+  return "unknown status";
+}
+
+int nvfp4_version(void) { return 100; }
+
+nvfp4_status nvfp4_device_check(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return (major == 10 && minor == 3) ? NVFP4_OK : NVFP4_ERR_ARCH;
+}
+
+nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  unsigned int code = 0;
+  nvfp4_status st = gemm_read_error(&code);
+  if (st != NVFP4_OK) return st;
+  return code ? NVFP4_ERR_DEVICE_TIMEOUT : NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize_sizes(int64_t rows, int64_t cols, int32_t mode, uint32_t flags,
+                                  size_t* codes_bytes, size_t* scales_bytes,
+                                  size_t* scales_t_bytes, size_t* workspace_bytes) {
+  if (mode < NVFP4_ROW_1X16 || mode > NVFP4_BLOCK_16X16) return NVFP4_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0) return NVFP4_ERR_SHAPE;
+  const int64_t orows = mode == NVFP4_COL_1X16 ? cols : rows;
+  const int64_t ocols = mode == NVFP4_COL_1X16 ? rows : cols;
+  if (ocols % 16) return NVFP4_ERR_SHAPE;
+  if (codes_bytes) *codes_bytes = (size_t)(orows * (ocols / 2));
+  if (scales_bytes) *scales_bytes = swizzled_scale_bytes(orows, ocols);
+  if (scales_t_bytes)
+    *scales_t_bytes = (flags & NVFP4_EMIT_T) && orows % 16 == 0
+                          ? swizzled_scale_bytes(ocols, orows) : 0;
+  if (workspace_bytes) *workspace_bytes = (flags & NVFP4_AMAX_GIVEN) ? 0 : kQuantWorkspaceBytes;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                            int64_t ld, int32_t mode, uint32_t flags, uint64_t seed,
+                            uint64_t offset, nvfp4_tensor* out, void* workspace,
+                            size_t workspace_bytes, nvfp4_stream stream) {
+  return quantize_impl(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, out, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                        int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                        int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                        nvfp4_stream stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return gemm_impl(A, a_view, B, b_view, D, d_mode, C, M, N, K, 0,
+                   static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm_ex(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                           int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                           int64_t N, int64_t K, int32_t tile_n, nvfp4_stream stream) {
+  return gemm_impl(A, a_view, B, b_view, D, d_mode, C, M, N, K, tile_n,
+                   static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

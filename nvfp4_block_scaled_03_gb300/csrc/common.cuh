@@ -1,0 +1,249 @@
+// common.cuh -- device helpers shared by the NVFP4 kernels (sm_103a only):
+// inline-PTX wrappers for mbarrier, TMA, tcgen05 and the FP4/FP8 conversion
+// instructions, the Philox4x32-10 counter RNG, and E4M3/E2M1 helpers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+
+#define NVFP4_DEV __device__ __forceinline__
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of the
+// published multiply-xor S-box; the key is bumped by the Weyl constants
+// between rounds.
+// ---------------------------------------------------------------------------
+NVFP4_DEV uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Stochastic-rounding words for the 4 consecutive output elements starting at
+// linear index idx4 (a multiple of 4): counter (idx4/4, stream 0, offset).
+NVFP4_DEV uint4 sr_words(uint64_t seed, uint64_t offset, uint64_t idx4) {
+  const uint64_t g = idx4 >> 2;
+  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), 0u, (uint32_t)offset),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// 16 RHT sign bits (bit i set -> sign -1): word 0 of counter (0, 0, 1, 0).
+NVFP4_DEV uint32_t rht_sign_bits(uint64_t seed) {
+  return philox4x32_10(make_uint4(0u, 0u, 1u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x &
+         0xFFFFu;
+}
+
+// ---------------------------------------------------------------------------
+// Format conversions.  E4M3 here is the FN variant (max 448, no infinity).
+// ---------------------------------------------------------------------------
+// RNE + saturation of one non-negative float to an E4M3 byte.
+NVFP4_DEV uint32_t e4m3_rn_satfinite(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;  // the second source lands in the low byte
+}
+
+// Exact value of an E4M3FN byte (no NaN expected: scales are finite).
+NVFP4_DEV float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float mag;
+  if (e == 0) mag = (float)m * 0.001953125f;  // m * 2^-9
+  else mag = __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -mag : mag;
+}
+
+// Two floats -> one byte of E2M1 codes with RNE and saturation to +-6:
+// `lo` goes to the low nibble (even element), `hi` to the high nibble.
+NVFP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+      : "=h"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// Stochastic rounding of y onto the E2M1 grid {0,.5,1,1.5,2,3,4,6}: rounds
+// |y| up to the next grid value iff r < floor(frac * 2^32), frac =
+// (|y| - lo) / (hi - lo) (exact: hi - lo is a power of two).  Returns the
+// 4-bit code, sign kept; |y| >= 6 saturates.
+NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
+  const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
+  const float a = fabsf(y);
+  if (!(a < 6.0f)) return sign | 7u;
+  const uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) +
+                      (a >= 4.0f);
+  // grid value and spacing to the next grid value for code lo
+  const float flo = lo < 4 ? 0.5f * (float)lo : (lo == 4 ? 2.0f : (lo == 5 ? 3.0f : 4.0f));
+  const float step = lo < 4 ? 0.5f : (lo == 6 ? 2.0f : 1.0f);
+  if (a == flo) return sign | lo;
+  const float frac = __fdiv_rn(__fsub_rn(a, flo), step);
+  const uint64_t thr = (uint64_t)__fmul_rn(frac, 4294967296.0f);  // exact, < 2^32
+  return sign | (((uint64_t)r < thr) ? lo + 1u : lo);
+}
+
+// Per-tensor encode scale from the amax: 6*448/amax, 1 for 0, FLT_MAX if the
+// quotient is not finite.
+NVFP4_DEV float per_tensor_s_enc(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  float s = __fdiv_rn(2688.0f, amax);
+  if (!isfinite(s)) s = 3.402823466e38f;
+  return s;
+}
+
+// Byte offset of (row r, scale column c) in the MMA scale layout of an
+// operand whose padded scale-column count is pc4 (a multiple of 4).
+NVFP4_DEV int64_t sf_offset(int64_t r, int64_t c, int64_t pc4) {
+  return ((r >> 7) * (pc4 >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+NVFP4_DEV float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// ---------------------------------------------------------------------------
+// Shared memory / mbarrier / TMA
+// ---------------------------------------------------------------------------
+NVFP4_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+NVFP4_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+NVFP4_DEV void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+NVFP4_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+NVFP4_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+NVFP4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+NVFP4_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+NVFP4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                           int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+NVFP4_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+NVFP4_DEV void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+NVFP4_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+NVFP4_DEV void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+NVFP4_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+NVFP4_DEV void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+NVFP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Arrive on `bar` once every tcgen05 operation this thread issued completes.
+NVFP4_DEV void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// Copy 32 rows x 128 bits of shared memory to tensor memory, replicated into
+// each of the four 32-lane quarters (the scale-factor copy).
+NVFP4_DEV void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// D(tmem) (+)= A(smem) . B(smem)^T with E2M1 operands and one UE4M3 scale per
+// 16 elements of K (scales in tensor memory); K = 64 per instruction.
+NVFP4_DEV void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
+// lane (quarter base + i), columns taddr.col .. +31.
+NVFP4_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+NVFP4_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:
+// rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked 1024 bytes apart.
+NVFP4_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                 // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+  return d;
+}
+// Descriptor of a 32-row x 16-byte scale-factor block (no swizzle, 8-row core
+// matrices of 128 contiguous bytes).
+NVFP4_DEV uint64_t smem_desc_sf(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;        // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf4nvf4: E2M1 A and B (K-major), UE4M3
+// scales, dense, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace nvfp4

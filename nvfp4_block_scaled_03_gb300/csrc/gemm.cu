@@ -1,0 +1,437 @@
+// gemm.cu -- NVFP4 block-scaled GEMM for sm_103a: D = alpha * A . B^T with
+// A [M, K], B [N, K] E2M1 K-major and one UE4M3 scale per 16 elements
+// ("NVFP4 pretraining recipe" page: FPROP, DGRAD and WGRAD consume NVFP4
+// inputs and emit BF16 outputs, Figure 1 text).
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: A/B code tiles (cp.async.bulk.tensor, 128-byte
+//               swizzle) and the scale atoms (cp.async.bulk, already in the
+//               MMA layout) into a STAGES-deep shared-memory ring;
+//   warp 1      allocates tensor memory; one thread copies each stage's scale
+//               atoms to tensor memory (tcgen05.cp) and issues
+//               tcgen05.mma.kind::mxf4nvf4.block_scale (K = 64 per
+//               instruction, 4 per stage), then tcgen05.commit frees the
+//               stage and, after the last K block, signals the accumulator;
+//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator (each warp its
+//               32-lane quarter), x alpha (= s_dec(A) * s_dec(B) read on the
+//               device), BF16 rounding, global stores.
+// Every mbarrier wait is bounded (2 s); on expiry the kernel records a code
+// in the device error word, the other roles stop at their next wait, copies
+// and MMAs in flight are drained (again bounded) and tensor memory is freed.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+static __device__ unsigned int g_gemm_error;
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr int kThreads = 192;
+constexpr int kBM = 128;            // rows of A per tile (one MMA, cta_group::1)
+constexpr int kBKBytes = 128;       // K bytes per stage (256 FP4 elements)
+constexpr int kAtomsPerStage = 4;   // scale atoms per 128 rows per stage (K = 256)
+constexpr uint32_t kTmemCols = 512;
+
+struct GemmArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* sdec_a;
+  const float* sdec_b;
+  void* D;
+  const void* C;
+  int M, N, K;
+  int kg;         // scale atoms per 128-row block along K (= K / 64)
+  int num_m_blk;  // ceil(M / 128)
+  int num_n_blk;  // ceil(N / BN)
+  int nrb_b;      // 128-row blocks of B's scale tensor (ceil(N / 128))
+};
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr uint32_t kA = kBM * kBKBytes;                 // 16 KB
+  static constexpr uint32_t kB = BN * kBKBytes;                  // 16/32 KB
+  static constexpr uint32_t kSFA = kAtomsPerStage * 512;          // 2 KB
+  static constexpr uint32_t kSFB = (BN / 128) * kAtomsPerStage * 512;
+  static constexpr uint32_t offA = 0;
+  static constexpr uint32_t offB = offA + STAGES * kA;
+  static constexpr uint32_t offSFA = offB + STAGES * kB;
+  static constexpr uint32_t offSFB = offSFA + STAGES * kSFA;
+  static constexpr uint32_t offBar = offSFB + STAGES * kSFB;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 3;  // full, empty, acc_full, acc_empty, drain
+  static constexpr uint32_t offMisc = offBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = offMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
+  // tensor memory columns: accumulator [0, BN), then per-stage scales
+  static constexpr uint32_t kSfCol0 = BN;
+  static constexpr uint32_t kSfColsPerStage = 16 + BN / 8;
+  static_assert(kSfCol0 + STAGES * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
+  static_assert(kAlloc <= 232448, "shared memory overflow");
+};
+
+NVFP4_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                            unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      atomicCAS(&g_gemm_error, 0u, code);
+      return false;
+    }
+  }
+}
+
+// Drain wait used after an abort: bounded, ignores the abort flag.
+NVFP4_DEV void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      atomicCAS(&g_gemm_error, 0u, 0xDEu);
+      return;
+    }
+  }
+}
+
+NVFP4_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int DMODE>
+NVFP4_DEV void store_row_chunk(const GemmArgs& a, int64_t row, int64_t col0, const uint32_t (&r)[32],
+                               float alpha) {
+  if (DMODE == NVFP4_D_BF16 || DMODE == NVFP4_D_BF16_ADD_C) {
+    __nv_bfloat16* D = static_cast<__nv_bfloat16*>(a.D) + row * a.N + col0;
+    const __nv_bfloat16* Cp = static_cast<const __nv_bfloat16*>(a.C) + row * a.N + col0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col0 + g * 8 >= a.N) break;
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(__uint_as_float(r[g * 8 + e]), alpha);
+      if (DMODE == NVFP4_D_BF16_ADD_C) {
+        const uint4 c = *reinterpret_cast<const uint4*>(Cp + g * 8);
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          f[2 * e] = __fadd_rn(f[2 * e], __uint_as_float(cw[e] << 16));
+          f[2 * e + 1] = __fadd_rn(f[2 * e + 1], __uint_as_float(cw[e] & 0xFFFF0000u));
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(f[0], f[1]);
+      o.y = pack_bf16x2(f[2], f[3]);
+      o.z = pack_bf16x2(f[4], f[5]);
+      o.w = pack_bf16x2(f[6], f[7]);
+      *reinterpret_cast<uint4*>(D + g * 8) = o;
+    }
+  } else {  // NVFP4_D_F32_ACCUM: D += float(bf16(alpha * acc))
+    float* D = static_cast<float*>(a.D) + row * a.N + col0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (col0 + g * 4 >= a.N) break;
+      float4 d = *reinterpret_cast<const float4*>(D + g * 4);
+      float t[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        t[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__uint_as_float(r[g * 4 + e]), alpha)));
+      d.x = __fadd_rn(d.x, t[0]);
+      d.y = __fadd_rn(d.y, t[1]);
+      d.z = __fadd_rn(d.z, t[2]);
+      d.w = __fadd_rn(d.w, t[3]);
+      *reinterpret_cast<float4*>(D + g * 4) = d;
+    }
+  }
+}
+
+template <int BN, int STAGES, int DMODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using L = Smem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::offBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t drain_bar = acc_full + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = (args.K + 255) / 256;
+  const int num_tiles = args.num_m_blk * args.num_n_blk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t s = 0, ph = 0;
+      int armed[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, 0x10u)) { ok = false; break; }
+          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          int nb_valid = 0;
+          for (int j = 0; j < BN / 128; ++j) nb_valid += (n_blk * (BN / 128) + j) < args.nrb_b;
+          const uint32_t sf_bytes = (uint32_t)natoms * 512u * (1u + (uint32_t)nb_valid);
+          mbar_arrive_expect_tx(full_bar(s), L::kA + L::kB + sf_bytes);
+          armed[s] = (int)ph;
+          tma_load_2d(sbase + L::offA + s * L::kA, &tmA, full_bar(s), kb * kBKBytes, m_blk * kBM);
+          tma_load_2d(sbase + L::offB + s * L::kB, &tmB, full_bar(s), kb * kBKBytes, n_blk * BN);
+          bulk_load(sbase + L::offSFA + s * L::kSFA,
+                    args.sfa + ((int64_t)m_blk * args.kg + kb * kAtomsPerStage) * 512,
+                    natoms * 512u, full_bar(s));
+          for (int j = 0; j < BN / 128; ++j) {
+            const int rb = n_blk * (BN / 128) + j;
+            if (rb < args.nrb_b)
+              bulk_load(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512),
+                        args.sfb + ((int64_t)rb * args.kg + kb * kAtomsPerStage) * 512,
+                        natoms * 512u, full_bar(s));
+          }
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        for (int i = 0; i < STAGES; ++i)
+          if (armed[i] >= 0) wait_drain(full_bar(i), (uint32_t)armed[i]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_nvf4(kBM, BN);
+      uint32_t s = 0, ph = 0, acc_ph = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!wait_bounded(acc_empty, acc_ph ^ 1u, abort_flag, 0x20u)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, 0x21u)) { ok = false; break; }
+          tc_fence_after();
+          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
+          const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
+          for (int j = 0; j < natoms; ++j) {
+            tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
+#pragma unroll
+            for (int b = 0; b < BN / 128; ++b)
+              tc_cp_32x128b_warpx4(sfb_t + j * (BN / 32) + 4 * b,
+                                   smem_desc_sf(sb + b * (kAtomsPerStage * 512) + j * 512));
+          }
+          const uint32_t a0 = sbase + L::offA + s * L::kA;
+          const uint32_t b0 = sbase + L::offB + s * L::kB;
+          for (int j = 0; j < natoms; ++j) {
+            tc_mma_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j), idesc,
+                        sfa_t + 4 * j, sfb_t + j * (BN / 32), (kb | j) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit(empty_bar(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_ph ^= 1u;
+      }
+      if (!ok && issued) {  // MMAs in flight must finish before tensor memory is freed
+        tc_commit(drain_bar);
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // this warp's 32-lane quarter of tensor memory
+    const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
+    uint32_t acc_ph = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+      if (!wait_bounded(acc_full, acc_ph, abort_flag, 0x30u)) break;
+      tc_fence_after();
+      const int64_t row = (int64_t)m_blk * kBM + q * 32 + lane;
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), r);
+        tmem_ld_wait();
+        const int64_t col0 = (int64_t)n_blk * BN + cc * 32;
+        if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r, alpha);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      acc_ph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host side -----------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a K-major code matrix [rows, kbytes] with a 128-byte x box_rows box.
+bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes,
+                   int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
+  const cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int DMODE>
+nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int sms,
+                    cudaStream_t stream) {
+  using L = Smem<BN, STAGES>;
+  auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE>;
+  static bool configured = false;  // attribute is per function; setting it twice is harmless
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    configured = true;
+  }
+  const int tiles = a.num_m_blk * a.num_n_blk;
+  const int grid = std::min(tiles, sms);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(ma, mb, a);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+template <int BN, int STAGES>
+nvfp4_status launch_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& mb,
+                         const GemmArgs& a, int sms, cudaStream_t s) {
+  switch (d_mode) {
+    case NVFP4_D_BF16: return launch<BN, STAGES, NVFP4_D_BF16>(ma, mb, a, sms, s);
+    case NVFP4_D_F32_ACCUM: return launch<BN, STAGES, NVFP4_D_F32_ACCUM>(ma, mb, a, sms, s);
+    default: return launch<BN, STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, a, sms, s);
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+nvfp4_status gemm_read_error(unsigned int* code) {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero)) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  *code = v;
+  return NVFP4_OK;
+}
+
+nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                       int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                       int64_t N, int64_t K, int32_t tile_n, cudaStream_t stream) {
+  if (!A || !B || !D) return NVFP4_ERR_INVALID_ARG;
+  if (a_view < 0 || a_view > 1 || b_view < 0 || b_view > 1) return NVFP4_ERR_INVALID_ARG;
+  if (d_mode < NVFP4_D_BF16 || d_mode > NVFP4_D_BF16_ADD_C) return NVFP4_ERR_INVALID_ARG;
+  if (d_mode == NVFP4_D_BF16_ADD_C && !C) return NVFP4_ERR_INVALID_ARG;
+  if (tile_n != 0 && tile_n != 128 && tile_n != 256) return NVFP4_ERR_INVALID_ARG;
+  const void* a_codes = a_view ? A->codes_t : A->codes;
+  const void* a_sf = a_view ? A->scales_t : A->scales;
+  const void* b_codes = b_view ? B->codes_t : B->codes;
+  const void* b_sf = b_view ? B->scales_t : B->scales;
+  if (!a_codes || !a_sf || !b_codes || !b_sf || !A->s_dec || !B->s_dec)
+    return NVFP4_ERR_INVALID_ARG;
+  const int64_t a_rows = a_view ? A->cols : A->rows, a_cols = a_view ? A->rows : A->cols;
+  const int64_t b_rows = b_view ? B->cols : B->rows, b_cols = b_view ? B->rows : B->cols;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 64 || N % 8) return NVFP4_ERR_SHAPE;
+  if (a_rows != M || b_rows != N || a_cols != K || b_cols != K) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(a_sf) || !aligned16(b_sf) ||
+      !aligned16(D) || (C && !aligned16(C)))
+    return NVFP4_ERR_ALIGN;
+
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+
+  const int bn = tile_n ? tile_n : (N <= 128 ? 128 : 256);
+  CUtensorMap ma, mb;
+  if (!make_code_map(&ma, a_codes, M, K / 2, kBM) || !make_code_map(&mb, b_codes, N, K / 2, bn))
+    return NVFP4_ERR_CUDA;
+
+  GemmArgs a;
+  a.sfa = static_cast<const uint8_t*>(a_sf);
+  a.sfb = static_cast<const uint8_t*>(b_sf);
+  a.sdec_a = A->s_dec;
+  a.sdec_b = B->s_dec;
+  a.D = D;
+  a.C = C;
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.kg = (int)(K / 64);
+  a.num_m_blk = (int)((M + kBM - 1) / kBM);
+  a.num_n_blk = (int)((N + bn - 1) / bn);
+  a.nrb_b = (int)((N + 127) / 128);
+  if (bn == 256) return launch_mode<256, 4>(d_mode, ma, mb, a, dev.sm_count, stream);
+  return launch_mode<128, 6>(d_mode, ma, mb, a, dev.sm_count, stream);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,49 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int major, minor;
+};
+
+// Cached attributes of the current device; NVFP4_ERR_ARCH if it is not sm_103.
+nvfp4_status current_device(DeviceInfo* info);
+
+// Partial maxima slots in a quantiser workspace (one float per amax CTA).
+constexpr int kMaxPartials = 1024;
+constexpr size_t kQuantWorkspaceBytes = kMaxPartials * sizeof(float);
+
+size_t swizzled_scale_bytes(int64_t rows, int64_t cols);
+
+nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                           int64_t ld, int32_t mode, uint32_t flags, uint64_t seed,
+                           uint64_t offset, nvfp4_tensor* out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
+                       int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
+                       int64_t N, int64_t K, int32_t tile_n, cudaStream_t stream);
+
+// Reads and clears the GEMM kernels' device error word (after a sync).
+nvfp4_status gemm_read_error(unsigned int* code);
+
+nvfp4_status swiglu_fwd_impl(const void* G, const void* U, void* H, int64_t n,
+                             cudaStream_t stream);
+nvfp4_status swiglu_bwd_impl(const void* dH, const void* G, const void* U, void* dG, void* dU,
+                             int64_t n, cudaStream_t stream);
+
+inline nvfp4_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,214 @@
+// mlp.cu -- SwiGLU MLP forward / backward with NVFP4 GEMMs: the host-side
+// sequence of quantiser, GEMM and SwiGLU launches on one stream, with the
+// caller's saved-activation buffer and workspace carved into the operands
+// ("NVFP4 pretraining recipe" page, Figure 1 text: the three MLP GEMMs of
+// each projection consume NVFP4 inputs and emit BF16; BF16 weight gradients
+// are folded into the FP32 master gradient).
+//
+// Per-operand recipe (bullets 3-5): X, H row-wise RNE for FPROP; W 16x16 RNE
+// with its transpose for DGRAD; dY, dG, dU row-wise SR for DGRAD; the WGRAD
+// operands X^T, H^T, dY^T, dG^T, dU^T column-wise, with the RHT (one sign
+// vector per seed, shared by every WGRAD pair) when flags has NVFP4_RHT, RNE
+// for activations and SR for gradients.  SR offsets: 8*step + 0..5 for
+// dY row/col, dG row/col, dU row/col.
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+// One quantised operand carved from a buffer.
+void carve_q(Carver& c, nvfp4_tensor* t, int64_t rows, int64_t cols, int32_t mode, bool emit_t) {
+  size_t codes = 0, sc = 0, sct = 0;
+  nvfp4_quantize_sizes(rows, cols, mode, emit_t ? NVFP4_EMIT_T : 0u, &codes, &sc, &sct, nullptr);
+  t->codes = c.take(codes);
+  t->scales = c.take(sc);
+  t->codes_t = emit_t ? c.take(codes) : nullptr;
+  t->scales_t = emit_t ? c.take(sct) : nullptr;
+  t->amax = static_cast<float*>(c.take(sizeof(float)));
+  t->s_dec = static_cast<float*>(c.take(sizeof(float)));
+  t->rows = t->cols = 0;
+  t->mode = mode;
+  t->flags = 0;
+}
+
+struct Saved {
+  nvfp4_tensor qWg, qWu, qWd, qXc, qHc;
+  void* G;
+  void* U;
+};
+struct Work {
+  void* partials;
+  nvfp4_tensor qX, qH, qdY, qdYc, qdG, qdGc, qdU, qdUc;
+  void* H;
+  void* dH;
+  void* dG;
+  void* dU;
+  void* dXg;
+};
+
+void carve_saved(void* base, int64_t M, int64_t D, int64_t F, Saved* s, size_t* bytes) {
+  Carver c(base);
+  carve_q(c, &s->qWg, F, D, NVFP4_BLOCK_16X16, true);
+  carve_q(c, &s->qWu, F, D, NVFP4_BLOCK_16X16, true);
+  carve_q(c, &s->qWd, D, F, NVFP4_BLOCK_16X16, true);
+  carve_q(c, &s->qXc, M, D, NVFP4_COL_1X16, false);
+  carve_q(c, &s->qHc, M, F, NVFP4_COL_1X16, false);
+  s->G = c.take((size_t)(M * F * 2));
+  s->U = c.take((size_t)(M * F * 2));
+  *bytes = c.off;
+}
+
+void carve_work(void* base, int64_t M, int64_t D, int64_t F, Work* w, size_t* bytes) {
+  Carver c(base);
+  w->partials = c.take(kQuantWorkspaceBytes);
+  carve_q(c, &w->qX, M, D, NVFP4_ROW_1X16, false);
+  carve_q(c, &w->qH, M, F, NVFP4_ROW_1X16, false);
+  carve_q(c, &w->qdY, M, D, NVFP4_ROW_1X16, false);
+  carve_q(c, &w->qdYc, M, D, NVFP4_COL_1X16, false);
+  carve_q(c, &w->qdG, M, F, NVFP4_ROW_1X16, false);
+  carve_q(c, &w->qdGc, M, F, NVFP4_COL_1X16, false);
+  carve_q(c, &w->qdU, M, F, NVFP4_ROW_1X16, false);
+  carve_q(c, &w->qdUc, M, F, NVFP4_COL_1X16, false);
+  w->H = c.take((size_t)(M * F * 2));
+  w->dH = c.take((size_t)(M * F * 2));
+  w->dG = c.take((size_t)(M * F * 2));
+  w->dU = c.take((size_t)(M * F * 2));
+  w->dXg = c.take((size_t)(M * D * 2));
+  *bytes = c.off;
+}
+
+bool dims_ok(int64_t M, int64_t D, int64_t F) {
+  return M > 0 && D > 0 && F > 0 && M % 128 == 0 && D % 128 == 0 && F % 128 == 0;
+}
+
+#define NVFP4_TRY(expr)                     \
+  do {                                      \
+    nvfp4_status _s = (expr);               \
+    if (_s != NVFP4_OK) return _s;          \
+  } while (0)
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+nvfp4_status nvfp4_mlp_sizes(int64_t M, int64_t D, int64_t F, size_t* saved_bytes,
+                             size_t* workspace_bytes) {
+  if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
+  Saved s;
+  Work w;
+  size_t sb = 0, wb = 0;
+  carve_saved(nullptr, M, D, F, &s, &sb);
+  carve_work(nullptr, M, D, F, &w, &wb);
+  if (saved_bytes) *saved_bytes = sb;
+  if (workspace_bytes) *workspace_bytes = wb;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, void* saved,
+                           size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                           nvfp4_stream stream) {
+  if (!p || !X || !Y || !saved || !workspace || !p->Wg || !p->Wu || !p->Wd)
+    return NVFP4_ERR_INVALID_ARG;
+  if (p->flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  const int64_t M = p->M, D = p->D, F = p->F;
+  if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
+  Saved s;
+  Work w;
+  size_t sb = 0, wb = 0;
+  carve_saved(saved, M, D, F, &s, &sb);
+  carve_work(workspace, M, D, F, &w, &wb);
+  if (saved_bytes < sb || workspace_bytes < wb) return NVFP4_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t rht = p->flags & NVFP4_RHT;
+  void* ws = w.partials;
+  const size_t wsb = kQuantWorkspaceBytes;
+
+  NVFP4_TRY(quantize_impl(p->Wg, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
+                          &s.qWg, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(p->Wu, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
+                          &s.qWu, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(p->Wd, NVFP4_IN_FP32, D, F, F, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
+                          &s.qWd, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(X, NVFP4_IN_BF16, M, D, D, NVFP4_ROW_1X16, 0, p->seed, 0, &w.qX, ws,
+                          wsb, st));
+  NVFP4_TRY(quantize_impl(X, NVFP4_IN_BF16, M, D, D, NVFP4_COL_1X16, rht, p->seed, 0, &s.qXc, ws,
+                          wsb, st));
+  NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWg, 0, s.G, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
+  NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWu, 0, s.U, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
+  NVFP4_TRY(swiglu_fwd_impl(s.G, s.U, w.H, M * F, st));
+  NVFP4_TRY(quantize_impl(w.H, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, 0, p->seed, 0, &w.qH, ws,
+                          wsb, st));
+  NVFP4_TRY(quantize_impl(w.H, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht, p->seed, 0, &s.qHc,
+                          ws, wsb, st));
+  NVFP4_TRY(gemm_impl(&w.qH, 0, &s.qWd, 0, Y, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void* saved,
+                           void* dX, float* dWg, float* dWu, float* dWd, void* workspace,
+                           size_t workspace_bytes, nvfp4_stream stream) {
+  if (!p || !dY || !saved || !dX || !dWg || !dWu || !dWd || !workspace)
+    return NVFP4_ERR_INVALID_ARG;
+  if (p->flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  const int64_t M = p->M, D = p->D, F = p->F;
+  if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
+  Saved s;
+  Work w;
+  size_t sb = 0, wb = 0;
+  carve_saved(const_cast<void*>(saved), M, D, F, &s, &sb);
+  carve_work(workspace, M, D, F, &w, &wb);
+  if (workspace_bytes < wb) return NVFP4_ERR_WORKSPACE;
+  // the saved operands' shapes (written by the forward's quantiser calls)
+  s.qWg.rows = F; s.qWg.cols = D;
+  s.qWu.rows = F; s.qWu.cols = D;
+  s.qWd.rows = D; s.qWd.cols = F;
+  s.qXc.rows = D; s.qXc.cols = M;
+  s.qHc.rows = F; s.qHc.cols = M;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t rht = p->flags & NVFP4_RHT;
+  const uint64_t o = 8 * p->step;
+  void* ws = w.partials;
+  const size_t wsb = kQuantWorkspaceBytes;
+
+  NVFP4_TRY(quantize_impl(dY, NVFP4_IN_BF16, M, D, D, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 0,
+                          &w.qdY, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(dY, NVFP4_IN_BF16, M, D, D, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
+                          o + 1, &w.qdYc, ws, wsb, st));
+  // DGRAD of the down projection: dH = dY . Wd  (Wd read through its transpose)
+  NVFP4_TRY(gemm_impl(&w.qdY, 0, &s.qWd, 1, w.dH, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
+  // WGRAD of the down projection: dWd += dY^T . H
+  NVFP4_TRY(gemm_impl(&w.qdYc, 0, &s.qHc, 0, dWd, NVFP4_D_F32_ACCUM, nullptr, D, F, M, 0, st));
+  NVFP4_TRY(swiglu_bwd_impl(w.dH, s.G, s.U, w.dG, w.dU, M * F, st));
+  NVFP4_TRY(quantize_impl(w.dG, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 2,
+                          &w.qdG, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(w.dG, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
+                          o + 3, &w.qdGc, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(w.dU, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 4,
+                          &w.qdU, ws, wsb, st));
+  NVFP4_TRY(quantize_impl(w.dU, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
+                          o + 5, &w.qdUc, ws, wsb, st));
+  // DGRAD of gate and up: dX = dG . Wg + dU . Wu (second GEMM adds the first)
+  NVFP4_TRY(gemm_impl(&w.qdG, 0, &s.qWg, 1, w.dXg, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
+  NVFP4_TRY(gemm_impl(&w.qdU, 0, &s.qWu, 1, dX, NVFP4_D_BF16_ADD_C, w.dXg, M, D, F, 0, st));
+  // WGRAD of gate and up: dWg += dG^T . X, dWu += dU^T . X
+  NVFP4_TRY(gemm_impl(&w.qdGc, 0, &s.qXc, 0, dWg, NVFP4_D_F32_ACCUM, nullptr, F, D, M, 0, st));
+  NVFP4_TRY(gemm_impl(&w.qdUc, 0, &s.qXc, 0, dWu, NVFP4_D_F32_ACCUM, nullptr, F, D, M, 0, st));
+  return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,141 @@
+"""GPU parity of the quantisers against the CPU oracle: codes, MMA-layout
+scales (with padding), amax and s_dec bit for bit."""
+import numpy as np
+import pytest
+
+from nvfp4_block_scaled_03_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from nvfp4_block_scaled_03_gb300 import binding
+    return binding
+
+
+import gpu_helpers as H  # noqa: E402
+
+# (mode name, flags) in both libraries' terms
+MODES = [
+    ("ROW", 0), ("ROW", "SR"), ("ROW", "RHT"), ("ROW", "RHT|SR"),
+    ("COL", 0), ("COL", "SR"), ("COL", "RHT"), ("COL", "RHT|SR"),
+    ("BLK", "EMIT_T"), ("BLK", "SR|EMIT_T"), ("BLK", 0),
+]
+
+
+def _mode(lib, name):
+    return {"ROW": lib.ROW_1X16, "COL": lib.COL_1X16, "BLK": lib.BLOCK_16X16}[name]
+
+
+def _flags(lib, spec):
+    if not spec:
+        return 0
+    f = 0
+    for part in spec.split("|"):
+        f |= getattr(lib, part)
+    return f
+
+
+def _input(shape, kind, dtype):
+    if kind == "x":
+        a = syn.activations(shape, seed=1)
+    elif kind == "w":
+        a = syn.weights(shape, seed=2)
+    else:
+        a = syn.gradients(shape, seed=3)
+    if dtype == "fp32":
+        a = syn.bf16_bits_to_f32(a) * np.float32(1.0 + 2.0 ** -12)  # not bf16-representable
+    return a
+
+
+def _run(nv, orc, x, mode_name, spec, seed=7, offset=3):
+    xt = H.dev_bf16(x) if x.dtype == np.uint16 else H.dev_f32(x)
+    q = nv.nvfp4_quantize(xt, _mode(nv, mode_name), _flags(nv, spec), seed=seed, offset=offset)
+    o = orc.quantize(x, _mode(orc, mode_name), _flags(orc, spec), seed=seed, offset=offset)
+    H.assert_quant_equal(q, o, f"{mode_name}/{spec}/{x.shape}")
+
+
+@pytest.mark.parametrize("mode_name,spec", MODES)
+@pytest.mark.parametrize("shape,kind", [((128, 256), "x"), ((512, 256), "w"), ((128, 512), "dy"),
+                                        ((208, 80), "x"), ((16, 16), "dy"), ((48, 32), "x"),
+                                        ((336, 400), "dy")])
+def test_quantize_small(nv, orc, mode_name, spec, shape, kind):
+    _run(nv, orc, _input(shape, kind, "bf16"), mode_name, spec)
+
+
+@pytest.mark.parametrize("mode_name,spec", [("ROW", 0), ("COL", "RHT|SR"), ("BLK", "EMIT_T"),
+                                            ("BLK", "SR|EMIT_T")])
+def test_quantize_fp32_input(nv, orc, mode_name, spec):
+    _run(nv, orc, _input((256, 384), "w", "fp32"), mode_name, spec)
+
+
+def test_quantize_amax_given_and_zero(nv, orc):
+    import torch
+    x = _input((128, 256), "x", "bf16")
+    big = float(np.abs(syn.bf16_bits_to_f32(x)).max()) * 3.0
+    q = nv.nvfp4_quantize(H.dev_bf16(x), nv.ROW_1X16, amax=big)
+    o = orc.quantize(x, orc.ROW_1X16, amax_given=big)
+    H.assert_quant_equal(q, o, "amax_given")
+    z = np.zeros((64, 64), np.uint16)
+    q = nv.nvfp4_quantize(H.dev_bf16(z), nv.COL_1X16, nv.RHT | nv.SR, seed=1)
+    o = orc.quantize(z, orc.COL_1X16, orc.RHT | orc.SR, seed=1)
+    H.assert_quant_equal(q, o, "zeros")
+    assert float(q.s_dec.cpu()[0]) == 1.0
+    torch.cuda.synchronize()
+
+
+def test_quantize_rejects_bad_shapes(nv):
+    import torch
+    x = torch.zeros(40, 24, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_quantize(x, nv.ROW_1X16)            # 24 % 16
+    assert e.value.status == nv.ERR_SHAPE
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_quantize(x, nv.COL_1X16)            # 40 % 16
+    assert e.value.status == nv.ERR_SHAPE
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_quantize(torch.zeros(32, 32, dtype=torch.bfloat16, device="cuda"),
+                          nv.BLOCK_16X16, nv.RHT)
+    assert e.value.status == nv.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape,kind,mode_name,spec", [
+    ((8192, 4096), "x", "ROW", 0),             # FPROP X
+    ((8192, 4096), "x", "COL", "RHT"),         # WGRAD X^T
+    ((14336, 4096), "w", "BLK", "EMIT_T"),     # W for FPROP and DGRAD
+    ((8192, 14336), "dy", "ROW", "SR"),        # DGRAD dY
+    ((8192, 14336), "dy", "COL", "RHT|SR"),    # WGRAD dY^T
+])
+def test_quantize_llama8b_full(nv, orc, shape, kind, mode_name, spec):
+    """The bench workload's quantiser calls at full size, every byte compared."""
+    _run(nv, orc, _input(shape, kind, "bf16"), mode_name, spec, seed=0, offset=1)
+
+
+@pytest.mark.parametrize("mode_name,spec", [("ROW", 0), ("COL", "RHT|SR")])
+def test_quantize_32k_tokens_sampled(nv, orc, mode_name, spec):
+    """[32768, 14336]: the GPU quantises the whole tensor; the oracle computes
+    the tensor amax itself and quantises 128-row output slabs with it."""
+    R, Cn = 32768, 14336
+    x = syn.activations((R, Cn), seed=5)
+    mode, flags = _mode(orc, mode_name), _flags(orc, spec)
+    q = nv.nvfp4_quantize(H.dev_bf16(x), _mode(nv, mode_name), _flags(nv, spec), seed=2, offset=4)
+    amax = orc.amax(x, mode, flags & orc.RHT, seed=2)
+    assert q.amax.cpu().numpy()[0] == amax
+    orows, ocols = orc.out_shape(mode, R, Cn)
+    codes = q.codes.cpu().numpy().reshape(orows, ocols // 2)
+    scales = q.scales.cpu().numpy()
+    atom_bytes = ((ocols // 16 + 3) // 4) * 512
+    rng = np.random.Generator(np.random.PCG64(9))
+    for rb in sorted(set(rng.integers(0, orows // 128, 3).tolist()) | {orows // 128 - 1}):
+        sl = slice(rb * 128, rb * 128 + 128)
+        xs = np.ascontiguousarray(x[sl] if mode == orc.ROW_1X16 else x[:, sl])
+        # the slab's own SR counters start at its first element: compare codes
+        # only for RNE; for SR compare the scales and the amax-derived s_dec
+        o = orc.quantize(xs, mode, flags & ~orc.SR, seed=2, offset=4, amax_given=float(amax))
+        assert np.array_equal(scales[rb * atom_bytes:(rb + 1) * atom_bytes], o["scales_sw"])
+        if not flags & orc.SR:
+            assert np.array_equal(codes[sl], o["codes"])
