@@ -1,0 +1,417 @@
+"""Benchmark of the NVFP4 linear-layer hot path on GB300.
+
+One step = one pass of the whole path over the Llama-3-8B MLP up/gate
+projection (M = 8192 tokens, K = 4096, N = 14336, synthetic seeded inputs
+resident in HBM): quantise X (1x16 RNE for FPROP, column-wise 1x16 + RHT for
+WGRAD), W (16x16 RNE + transpose), dY (1x16 SR for DGRAD, column-wise RHT+SR
+for WGRAD), then the FPROP, DGRAD and WGRAD block-scaled GEMMs to BF16.
+
+Prints one JSON line: value = GEMM FLOPs of the step (3 x 2MNK) / step time,
+aggregated over ranks; plus the GEMM roofline (tensor-bound, FP4 peak =
+measured bf16 peak x the nominal fp4/bf16 ratio 6), the quantisers' GB/s
+against the measured HBM copy bandwidth, an end-to-end figure through host
+buffers, the oracle's CPU baseline and sampled SM clocks.
+
+Multi-GPU: replicas only (one independent replica per rank, launched by
+torchrun); the timing is max over ranks.  ``--impl reference`` times the CPU
+oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roofline"
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
+        "dY ~ N(0,1e-3), bf16")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=500)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--m", type=int, default=8192)
+    p.add_argument("--k", type=int, default=4096)
+    p.add_argument("--n", type=int, default=14336)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; gloo works for the CPU tests)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.5)
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: power above the midpoint of the range seen
+        thr = (min(power) + max(power)) / 2 if power else 0
+        loaded = [s for s, p in zip(sm, power) if p >= thr] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# the step
+# ---------------------------------------------------------------------------
+class Layer:
+    """Device buffers of one linear layer's hot path, allocated once."""
+
+    def __init__(self, M, K, N, device):
+        import torch
+
+        from nvfp4_block_scaled_03_gb300 import binding as nv
+        from nvfp4_block_scaled_03_gb300 import synthetic as syn
+        self.nv, self.M, self.K, self.N = nv, M, K, N
+        X, W, dY = syn.linear_layer(M, K, N)
+        self.host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                     for k, v in (("X", X), ("W", W), ("dY", dY))}
+        self.X = self.host["X"].to(device)
+        self.W = self.host["W"].to(device)
+        self.dY = self.host["dY"].to(device)
+        self.qX = nv.alloc_qtensor(M, K, nv.ROW_1X16, device=device)
+        self.qXc = nv.alloc_qtensor(M, K, nv.COL_1X16, device=device)
+        self.qW = nv.alloc_qtensor(N, K, nv.BLOCK_16X16, nv.EMIT_T, device=device)
+        self.qdY = nv.alloc_qtensor(M, N, nv.ROW_1X16, device=device)
+        self.qdYc = nv.alloc_qtensor(M, N, nv.COL_1X16, device=device)
+        self.ws = torch.empty(nv.quantize_sizes(M, K, 0)[3], dtype=torch.uint8, device=device)
+        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty(N, K, dtype=torch.bfloat16, device=device)
+        self.out_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                         for k, v in (("Y", self.Y), ("dX", self.dX), ("dW", self.dW))}
+        self.launches_per_step = 5 * 2 + 3
+        self.names = ["q_x_row", "q_x_col_rht", "q_w_16x16", "q_dy_row_sr", "q_dy_col_rht_sr",
+                      "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
+
+    def flops(self):
+        return 3 * 2.0 * self.M * self.N * self.K
+
+    def quant_bytes(self):
+        """Algorithmic bytes of the five quantiser calls (amax pre-pass
+        excluded): read the bf16 input once, write codes and scales."""
+        M, K, N = self.M, self.K, self.N
+        b = 0
+        for rows, cols, t in ((M, K, 1), (M, K, 1), (N, K, 2), (M, N, 1), (M, N, 1)):
+            elts = rows * cols
+            b += 2 * elts + elts / 2 * t + (elts / 16 if t == 1 else 2 * elts / 256)
+        return b
+
+    def step(self, events=None):
+        nv = self.nv
+        calls = [
+            lambda: nv.nvfp4_quantize(self.X, nv.ROW_1X16, 0, out=self.qX, workspace=self.ws),
+            lambda: nv.nvfp4_quantize(self.X, nv.COL_1X16, nv.RHT, seed=0, out=self.qXc,
+                                      workspace=self.ws),
+            lambda: nv.nvfp4_quantize(self.W, nv.BLOCK_16X16, nv.EMIT_T, out=self.qW,
+                                      workspace=self.ws),
+            lambda: nv.nvfp4_quantize(self.dY, nv.ROW_1X16, nv.SR, seed=0, offset=0,
+                                      out=self.qdY, workspace=self.ws),
+            lambda: nv.nvfp4_quantize(self.dY, nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1,
+                                      out=self.qdYc, workspace=self.ws),
+            lambda: nv.nvfp4_gemm(self.qX, self.qW, out=self.Y),
+            lambda: nv.nvfp4_gemm(self.qdY, self.qW, b_view=1, out=self.dX),
+            lambda: nv.nvfp4_gemm(self.qdYc, self.qXc, out=self.dW),
+        ]
+        for i, c in enumerate(calls):
+            if events is not None:
+                events[i][0].record()
+            c()
+            if events is not None:
+                events[i][1].record()
+
+
+def run_ours(args):
+    import torch
+    world, rank = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+
+    layer = Layer(args.m, args.k, args.n, device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        layer.step()
+    nv.check_device_errors()
+    torch.cuda.synchronize()
+
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layer.names]
+          for _ in range(args.steps)]
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)  # evict the previous step's data from L2 (untimed)
+        step_ev[s][0].record(stream)
+        layer.step(ev[s])
+        step_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop() if rank == 0 else None
+    nv.check_device_errors()
+
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = max_over_ranks(sum(step_ms), device)
+    kern_ms = {name: statistics.mean(e[i][0].elapsed_time(e[i][1]) for e in ev)
+               for i, name in enumerate(layer.names)}
+    ms_per_step = total_ms / args.steps
+    value = world * layer.flops() / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through host buffers (H2D inputs, D2H outputs) ----------
+    h2d = sum(t.numel() * t.element_size() for t in layer.host.values())
+    d2h = sum(t.numel() * t.element_size() for t in layer.out_host.values())
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        layer.X.copy_(layer.host["X"], non_blocking=True)
+        layer.W.copy_(layer.host["W"], non_blocking=True)
+        layer.dY.copy_(layer.host["dY"], non_blocking=True)
+        layer.step()
+        layer.out_host["Y"].copy_(layer.Y, non_blocking=True)
+        layer.out_host["dX"].copy_(layer.dX, non_blocking=True)
+        layer.out_host["dW"].copy_(layer.dW, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, device)
+    e2e_value = world * layer.flops() / e2e_s / 1e12
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    gemm_ms = statistics.mean(kern_ms[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
+    gemm_flops = 2.0 * args.m * args.n * args.k
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    q_ms = sum(kern_ms[k] for k in layer.names if k.startswith("q_"))
+    q_gbs = layer.quant_bytes() / (q_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": DATA,
+        "config": {"workload": "Llama-3-8B MLP up/gate projection, one pass (quantise X, W, dY; "
+                               "FPROP, DGRAD, WGRAD to BF16)",
+                   "M": args.m, "K": args.k, "N": args.n,
+                   "l2": "flushed (256 MiB device write, untimed) before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4 (mean of FPROP/DGRAD/WGRAD)",
+                     "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
+                     "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)",
+                     "traffic": None},
+        "quantize": {"gbs": round(q_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+                     "frac": round(q_gbs / peaks["hbm_gbs"], 4),
+                     "ms_per_step": round(q_ms, 4),
+                     "bytes_per_step": int(layer.quant_bytes()),
+                     "note": "algorithmic bytes (bf16 read + codes + scales) over quantiser "
+                             "time including the amax pre-pass"},
+        "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": layer.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def oracle_step(X, W, dY, orc):
+    qX = orc.quantize(X, orc.ROW_1X16)
+    qXc = orc.quantize(X, orc.COL_1X16, orc.RHT, seed=0)
+    qW = orc.quantize(W, orc.BLOCK_16X16, orc.EMIT_T)
+    qdY = orc.quantize(dY, orc.ROW_1X16, orc.SR, seed=0, offset=0)
+    qdYc = orc.quantize(dY, orc.COL_1X16, orc.RHT | orc.SR, seed=0, offset=1)
+    orc.gemm_fp64(qX, qW)
+    orc.gemm_fp64(qdY, orc.transposed_view(qW))
+    orc.gemm_fp64(qdYc, qXc)
+
+
+def cpu_baseline(args, m_sample=32):
+    import oracle as orc
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    orc.build()
+    X, W, dY = syn.linear_layer(m_sample, args.k, args.n)
+    t0 = time.perf_counter()
+    oracle_step(X, W, dY, orc)
+    dt = time.perf_counter() - t0
+    flops = 3 * 2.0 * m_sample * args.n * args.k
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"one full step of the workload with M = {m_sample} tokens (K = {args.k}, "
+                      f"N = {args.n}, full weight): {dt:.1f} s single-threaded C oracle "
+                      f"(FP64 GEMMs)"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the full step of the
+    workload on a bounded sample (16 tokens x 256 output features, K = 4096),
+    so that --steps K --warmup W ends within a few minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as orc
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    orc.build()
+    m_s, n_s = 16, 256
+    X, W, dY = syn.linear_layer(m_s, args.k, n_s)
+    for _ in range(args.warmup):
+        oracle_step(X, W, dY, orc)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(X, W, dY, orc)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    flops = 3 * 2.0 * m_s * n_s * args.k
+    value = flops / dt / 1e12
+    sample = (f"each step: quantise + FPROP/DGRAD/WGRAD on M = {m_s} tokens x N = {n_s} output "
+              f"features (K = {args.k}) of the workload, single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle GEMM), f32 (oracle quantiser)", "data": DATA,
+        "config": {"workload": "Llama-3-8B MLP up/gate projection, one pass", "M": args.m,
+                   "K": args.k, "N": args.n, "sample_M": m_s, "sample_N": n_s},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -77,21 +77,28 @@ NVFP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 
 // Stochastic rounding of y onto the E2M1 grid {0,.5,1,1.5,2,3,4,6}: rounds
 // |y| up to the next grid value iff r < floor(frac * 2^32), frac =
-// (|y| - lo) / (hi - lo) (exact: hi - lo is a power of two).  Returns the
-// 4-bit code, sign kept; |y| >= 6 saturates.
+// (|y| - lo) / (hi - lo).  Returns the 4-bit code, sign kept; |y| >= 6
+// saturates.  Evaluated exactly on the float's bits: for |y| >= 1 the grid
+// keeps one mantissa bit, so frac * 2^32 is the 22 mantissa bits below it
+// shifted left by 10; on [0.5, 1) it is the 23 mantissa bits << 9; below 0.5
+// it is floor(|y| * 2^33) (an exact power-of-two scaling).
 NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
-  const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
-  const float a = fabsf(y);
-  if (!(a < 6.0f)) return sign | 7u;
-  const uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) +
-                      (a >= 4.0f);
-  // grid value and spacing to the next grid value for code lo
-  const float flo = lo < 4 ? 0.5f * (float)lo : (lo == 4 ? 2.0f : (lo == 5 ? 3.0f : 4.0f));
-  const float step = lo < 4 ? 0.5f : (lo == 6 ? 2.0f : 1.0f);
-  if (a == flo) return sign | lo;
-  const float frac = __fdiv_rn(__fsub_rn(a, flo), step);
-  const uint64_t thr = (uint64_t)__fmul_rn(frac, 4294967296.0f);  // exact, < 2^32
-  return sign | (((uint64_t)r < thr) ? lo + 1u : lo);
+  const uint32_t bits = __float_as_uint(y);
+  const uint32_t sign = (bits >> 28) & 8u;
+  const uint32_t abits = bits & 0x7FFFFFFFu;
+  if (!(__uint_as_float(abits) < 6.0f)) return sign | 7u;
+  uint32_t code, thr;
+  if (abits >= 0x3F800000u) {  // [1, 6): binades [1,2), [2,4), [4,6)
+    code = ((((abits >> 23) - 127u) + 1u) << 1) | ((abits >> 22) & 1u);
+    thr = (abits & 0x3FFFFFu) << 10;
+  } else if (abits >= 0x3F000000u) {  // [0.5, 1)
+    code = 1u;
+    thr = (abits & 0x7FFFFFu) << 9;
+  } else {  // [0, 0.5)
+    code = 0u;
+    thr = __float2uint_rz(__fmul_rn(__uint_as_float(abits), 8589934592.0f));
+  }
+  return sign | (r < thr ? code + 1u : code);
 }
 
 // Per-tensor encode scale from the amax: 6*448/amax, 1 for 0, FLT_MAX if the

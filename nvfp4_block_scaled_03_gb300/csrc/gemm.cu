@@ -12,9 +12,11 @@
 //               tcgen05.mma.kind::mxf4nvf4.block_scale (K = 64 per
 //               instruction, 4 per stage), then tcgen05.commit frees the
 //               stage and, after the last K block, signals the accumulator;
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator (each warp its
-//               32-lane quarter), x alpha (= s_dec(A) * s_dec(B) read on the
-//               device), BF16 rounding, global stores.
+//   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulator (each warp one
+//               32-lane quarter and half of the columns) into registers,
+//               release of the accumulator to the MMA warp, then x alpha
+//               (= s_dec(A) * s_dec(B) read on the device), BF16 rounding
+//               and global stores while the next tile's MMAs run.
 // Every mbarrier wait is bounded (2 s); on expiry the kernel records a code
 // in the device error word, the other roles stop at their next wait, copies
 // and MMAs in flight are drained (again bounded) and tensor memory is freed.
@@ -31,7 +33,7 @@ static __device__ unsigned int g_gemm_error;
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kBM = 128;            // rows of A per tile (one MMA, cta_group::1)
 constexpr int kBKBytes = 128;       // K bytes per stage (256 FP4 elements)
 constexpr int kAtomsPerStage = 4;   // scale atoms per 128 rows per stage (K = 256)
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, 8);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -249,16 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
           const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
+          const uint32_t a0 = sbase + L::offA + s * L::kA;
+          const uint32_t b0 = sbase + L::offB + s * L::kB;
+          // per K step: its scale atoms to tensor memory, then its MMA, so the
+          // copies of step j+1 proceed while the MMA of step j runs
           for (int j = 0; j < natoms; ++j) {
             tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
 #pragma unroll
             for (int b = 0; b < BN / 128; ++b)
               tc_cp_32x128b_warpx4(sfb_t + j * (BN / 32) + 4 * b,
                                    smem_desc_sf(sb + b * (kAtomsPerStage * 512) + j * 512));
-          }
-          const uint32_t a0 = sbase + L::offA + s * L::kA;
-          const uint32_t b0 = sbase + L::offB + s * L::kB;
-          for (int j = 0; j < natoms; ++j) {
             tc_mma_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j), idesc,
                         sfa_t + 4 * j, sfb_t + j * (BN / 32), (kb | j) != 0 ? 1u : 0u);
           }
@@ -277,26 +279,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // this warp's 32-lane quarter of tensor memory
+    // Warp w reads lane quarter w % 4 of tensor memory and one half of the
+    // tile's columns.  It drains its part of the accumulator into registers,
+    // releases the accumulator to the MMA warp, then scales and stores.
+    constexpr int kCols = BN / 2, kChunks = kCols / 32;
+    const int q = warp & 3, h = (warp - 2) >> 2;
     const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
       if (!wait_bounded(acc_full, acc_ph, abort_flag, 0x30u)) break;
       tc_fence_after();
-      const int64_t row = (int64_t)m_blk * kBM + q * 32 + lane;
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), r);
-        tmem_ld_wait();
-        const int64_t col0 = (int64_t)n_blk * BN + cc * 32;
-        if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r, alpha);
-      }
+      uint32_t r[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kCols + c * 32), r[c]);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
       acc_ph ^= 1u;
+      const int64_t row = (int64_t)m_blk * kBM + q * 32 + lane;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int64_t col0 = (int64_t)n_blk * BN + h * kCols + c * 32;
+        if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r[c], alpha);
+      }
     }
   }
 
