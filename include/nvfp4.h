@@ -171,11 +171,19 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tenso
                         int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                         nvfp4_stream stream);
 
-/* As nvfp4_gemm with an explicit output tile width: tile_n = 128 or 256
- * (0 picks the default).  For tuning and tests. */
+/* Output-tile configurations of nvfp4_gemm_ex. */
+enum {
+  NVFP4_TILE_AUTO = 0,          /* 128 x 256 on one SM (128 x 128 when N <= 128)           */
+  NVFP4_TILE_128X128 = 1,       /* one SM per 128 x 128 tile                               */
+  NVFP4_TILE_128X256 = 2,       /* one SM per 128 x 256 tile                               */
+  NVFP4_TILE_PAIR_256X256 = 3   /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */
+};
+
+/* As nvfp4_gemm with an explicit output-tile configuration (NVFP4_TILE_*).
+ * For tuning and tests; results are identical up to FP32 summation order. */
 nvfp4_status nvfp4_gemm_ex(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                            int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
-                           int64_t N, int64_t K, int32_t tile_n, nvfp4_stream stream);
+                           int64_t N, int64_t K, int32_t tile, nvfp4_stream stream);
 
 /* ---------------------------------------------------------------------- */
 /* SwiGLU MLP (gate, up, down projections) with NVFP4 GEMMs                */

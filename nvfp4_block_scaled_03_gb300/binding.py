@@ -23,6 +23,7 @@ IN_BF16, IN_FP32 = 0, 1
 ROW_1X16, COL_1X16, BLOCK_16X16 = 0, 1, 2
 RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
 D_BF16, D_F32_ACCUM, D_BF16_ADD_C = 0, 1, 2
+TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256 = 0, 1, 2, 3
 
 
 class NVFP4Error(RuntimeError):
@@ -184,7 +185,7 @@ def nvfp4_quantize(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0, of
 
 def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,
                out: torch.Tensor | None = None, d_mode: int = D_BF16,
-               C_add: torch.Tensor | None = None, tile_n: int = 0, stream=None) -> torch.Tensor:
+               C_add: torch.Tensor | None = None, tile: int = TILE_AUTO, stream=None) -> torch.Tensor:
     """D = alpha * A . B^T (see nvfp4_gemm in nvfp4.h); returns D."""
     M = A.desc.cols if a_view else A.desc.rows
     K = A.desc.rows if a_view else A.desc.cols
@@ -193,9 +194,9 @@ def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,
         dtype = torch.float32 if d_mode == D_F32_ACCUM else torch.bfloat16
         out = (torch.zeros if d_mode == D_F32_ACCUM else torch.empty)(
             (M, N), dtype=dtype, device=A.codes.device)
-    if tile_n:
+    if tile:
         st = lib.nvfp4_gemm_ex(C.byref(A.desc), a_view, C.byref(B.desc), b_view, out.data_ptr(),
-                               d_mode, _ptr(C_add), M, N, K, tile_n, _stream(stream))
+                               d_mode, _ptr(C_add), M, N, K, tile, _stream(stream))
     else:
         st = lib.nvfp4_gemm(C.byref(A.desc), a_view, C.byref(B.desc), b_view, out.data_ptr(),
                             d_mode, _ptr(C_add), M, N, K, None, 0, _stream(stream))

@@ -106,8 +106,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tenso
 
 nvfp4_status nvfp4_gemm_ex(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                            int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
-                           int64_t N, int64_t K, int32_t tile_n, nvfp4_stream stream) {
-  return gemm_impl(A, a_view, B, b_view, D, d_mode, C, M, N, K, tile_n,
+                           int64_t N, int64_t K, int32_t tile, nvfp4_stream stream) {
+  return gemm_impl(A, a_view, B, b_view, D, d_mode, C, M, N, K, tile,
                    static_cast<cudaStream_t>(stream));
 }
 

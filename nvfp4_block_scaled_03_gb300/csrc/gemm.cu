@@ -316,6 +316,235 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// =============================================================================
+// CTA-pair kernel: output tiles of 256 x 256 computed by a cluster of two
+// CTAs with tcgen05 cta_group::2.  CTA r loads A rows [128 r, 128 r + 128)
+// and B rows [128 r, 128 r + 128) of the tile, the scale atoms of its A rows
+// and all scale atoms of the tile's B rows; every load completes on the
+// leader's (rank 0) full barrier.  The leader's MMA thread copies one K
+// step's scales ahead of the MMA that reads them and commits to the empty /
+// accumulator barriers of both CTAs.  Each CTA's epilogue drains its 128
+// accumulator rows and releases them on the leader's barrier.  Per SM this
+// moves two thirds of the operand bytes of the single-CTA 128 x 256 tile for
+// the same MMA work, and issues half the scale copies per FLOP.
+// =============================================================================
+constexpr int kPairBN = 256;
+
+template <int STAGES>
+struct PairSmem {
+  static constexpr uint32_t kA = 128 * kBKBytes;          // this CTA's 128 A rows
+  static constexpr uint32_t kB = 128 * kBKBytes;          // this CTA's 128 B rows
+  static constexpr uint32_t kSFA = kAtomsPerStage * 512;  // own A rows' scales
+  static constexpr uint32_t kSFB = 2 * kAtomsPerStage * 512;  // the tile's 256 B rows' scales
+  static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
+  static constexpr uint32_t offA = 0;
+  static constexpr uint32_t offB = offA + STAGES * kA;
+  static constexpr uint32_t offSFA = offB + STAGES * kB;
+  static constexpr uint32_t offSFB = offSFA + STAGES * kSFA;
+  static constexpr uint32_t offBar = offSFB + STAGES * kSFB;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 3;
+  static constexpr uint32_t offMisc = offBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = offMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static constexpr uint32_t kSfCol0 = kPairBN;
+  static constexpr uint32_t kSfColsPerStage = 16 + 32;
+  static_assert(kSfCol0 + STAGES * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
+  static_assert(kAlloc <= 232448, "shared memory overflow");
+};
+
+// Bounded wait for the pair: a timeout also raises the peer CTA's abort flag.
+NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                 uint32_t peer_abort_addr, unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      st_cluster_u32(peer_abort_addr, 1u);
+      atomicCAS(&g_gemm_error, 0u, code);
+      return false;
+    }
+  }
+}
+
+template <int STAGES, int DMODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmSFA,
+                          const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args) {
+  using L = PairSmem<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::offBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t drain_bar = acc_full + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + L::offMisc + 4), rank ^ 1u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = (args.K + 255) / 256;
+  const int num_tiles = args.num_m_blk * args.num_n_blk;  // 256 x 256 tiles
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmSFA);
+      prefetch_tmap(&tmSFB);
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+        const int a_rb = m_blk * 2 + (int)rank;  // this CTA's 128-row block of A
+        const int b_rb0 = n_blk * 2;             // the tile's first 128-row block of B
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded_pair(empty_bar(s), ph ^ 1u, abort_flag, peer_abort, 0x11u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(s), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), L::kStageTx);
+          tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
+          tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
+                           (b_rb0 + (int)rank) * 128);
+          // scale atoms as 128-byte rows: 4 atoms = 16 rows per 128 operand rows
+          tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
+                           (a_rb * args.kg + kb * kAtomsPerStage) * 4);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512), &tmSFB,
+                             fb, 0, ((b_rb0 + j) * args.kg + kb * kAtomsPerStage) * 4);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // give copies already issued time to land before exit
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_nvf4(256, kPairBN);
+      uint32_t s = 0, ph = 0, acc_ph = 0;
+      bool ok = true, issued = false;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        if (!wait_bounded_pair(acc_empty, acc_ph ^ 1u, abort_flag, peer_abort, 0x22u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded_pair(full_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
+          const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
+          const uint32_t a0 = sbase + L::offA + s * L::kA;
+          const uint32_t b0 = sbase + L::offB + s * L::kB;
+          auto copy_scales = [&](int j) {
+            tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
+            tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j, smem_desc_sf(sb + j * 512));
+            tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4,
+                                      smem_desc_sf(sb + kAtomsPerStage * 512 + j * 512));
+          };
+          copy_scales(0);
+          for (int j = 0; j < natoms; ++j) {
+            if (j + 1 < natoms) copy_scales(j + 1);  // next step's scales ahead of this MMA
+            tc_mma_pair_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
+                             idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_pair(empty_bar(s), 3);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair(acc_full, 3);
+        acc_ph ^= 1u;
+      }
+      if (!ok && issued) {
+        tc_commit_pair(drain_bar, 1);
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    constexpr int kCols = kPairBN / 2, kChunks = kCols / 32;
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
+    const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
+    uint32_t acc_ph = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+      if (!wait_bounded_pair(acc_full, acc_ph, abort_flag, peer_abort, 0x33u)) break;
+      tc_fence_after();
+      uint32_t r[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kCols + c * 32), r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      acc_ph ^= 1u;
+      const int64_t row = (int64_t)m_blk * 256 + rank * 128 + q * 32 + lane;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int64_t col0 = (int64_t)n_blk * kPairBN + h * kCols + c * 32;
+        if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r[c], alpha);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ---- host side -----------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -351,6 +580,58 @@ bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kby
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a scale tensor viewed as rows of 128 bytes (4 rows per atom),
+// box of 16 rows (the 4 atoms of one stage).
+bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int STAGES, int DMODE>
+nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
+                         const CUtensorMap& msb, const GemmArgs& a, int sms, cudaStream_t stream) {
+  using L = PairSmem<STAGES>;
+  auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    configured = true;
+  }
+  // persistent grid: as many pairs as can be resident at once (cluster
+  // placement can leave SMs of a GPC unpaired), at most one per tile
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+    max_pairs = std::min(n, sms / 2);
+  }
+  const int tiles = a.num_m_blk * a.num_n_blk;
+  const int grid = 2 * std::min(tiles, max_pairs);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(ma, mb, msa, msb, a);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 template <int BN, int STAGES, int DMODE>
 nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int sms,
                     cudaStream_t stream) {
@@ -379,6 +660,18 @@ nvfp4_status launch_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& m
   }
 }
 
+template <int STAGES>
+nvfp4_status launch_pair_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const CUtensorMap& msa, const CUtensorMap& msb, const GemmArgs& a,
+                              int sms, cudaStream_t s) {
+  switch (d_mode) {
+    case NVFP4_D_BF16: return launch_pair<STAGES, NVFP4_D_BF16>(ma, mb, msa, msb, a, sms, s);
+    case NVFP4_D_F32_ACCUM:
+      return launch_pair<STAGES, NVFP4_D_F32_ACCUM>(ma, mb, msa, msb, a, sms, s);
+    default: return launch_pair<STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, msa, msb, a, sms, s);
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -394,12 +687,12 @@ nvfp4_status gemm_read_error(unsigned int* code) {
 
 nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                        int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
-                       int64_t N, int64_t K, int32_t tile_n, cudaStream_t stream) {
+                       int64_t N, int64_t K, int32_t tile, cudaStream_t stream) {
   if (!A || !B || !D) return NVFP4_ERR_INVALID_ARG;
   if (a_view < 0 || a_view > 1 || b_view < 0 || b_view > 1) return NVFP4_ERR_INVALID_ARG;
   if (d_mode < NVFP4_D_BF16 || d_mode > NVFP4_D_BF16_ADD_C) return NVFP4_ERR_INVALID_ARG;
   if (d_mode == NVFP4_D_BF16_ADD_C && !C) return NVFP4_ERR_INVALID_ARG;
-  if (tile_n != 0 && tile_n != 128 && tile_n != 256) return NVFP4_ERR_INVALID_ARG;
+  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_PAIR_256X256) return NVFP4_ERR_INVALID_ARG;
   const void* a_codes = a_view ? A->codes_t : A->codes;
   const void* a_sf = a_view ? A->scales_t : A->scales;
   const void* b_codes = b_view ? B->codes_t : B->codes;
@@ -419,11 +712,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   nvfp4_status st = current_device(&dev);
   if (st != NVFP4_OK) return st;
 
-  const int bn = tile_n ? tile_n : (N <= 128 ? 128 : 256);
-  CUtensorMap ma, mb;
-  if (!make_code_map(&ma, a_codes, M, K / 2, kBM) || !make_code_map(&mb, b_codes, N, K / 2, bn))
-    return NVFP4_ERR_CUDA;
-
+  if (tile == NVFP4_TILE_AUTO) tile = N <= 128 ? NVFP4_TILE_128X128 : NVFP4_TILE_128X256;
   GemmArgs a;
   a.sfa = static_cast<const uint8_t*>(a_sf);
   a.sfb = static_cast<const uint8_t*>(b_sf);
@@ -435,9 +724,23 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   a.N = (int)N;
   a.K = (int)K;
   a.kg = (int)(K / 64);
+  a.nrb_b = (int)((N + 127) / 128);
+  CUtensorMap ma, mb;
+  if (tile == NVFP4_TILE_PAIR_256X256) {
+    CUtensorMap msa, msb;
+    if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
+        !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
+        !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
+      return NVFP4_ERR_CUDA;
+    a.num_m_blk = (int)((M + 255) / 256);
+    a.num_n_blk = (int)((N + 255) / 256);
+    return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, a, dev.sm_count, stream);
+  }
+  const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
+  if (!make_code_map(&ma, a_codes, M, K / 2, kBM) || !make_code_map(&mb, b_codes, N, K / 2, bn))
+    return NVFP4_ERR_CUDA;
   a.num_m_blk = (int)((M + kBM - 1) / kBM);
   a.num_n_blk = (int)((N + bn - 1) / bn);
-  a.nrb_b = (int)((N + 127) / 128);
   if (bn == 256) return launch_mode<256, 4>(d_mode, ma, mb, a, dev.sm_count, stream);
   return launch_mode<128, 6>(d_mode, ma, mb, a, dev.sm_count, stream);
 }

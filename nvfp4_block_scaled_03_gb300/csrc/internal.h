@@ -32,7 +32,7 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
 
 nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                        int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
-                       int64_t N, int64_t K, int32_t tile_n, cudaStream_t stream);
+                       int64_t N, int64_t K, int32_t tile, cudaStream_t stream);
 
 // Reads and clears the GEMM kernels' device error word (after a sync).
 nvfp4_status gemm_read_error(unsigned int* code);

@@ -43,16 +43,16 @@ def _gemms(orc, L):
     return {"FPROP": (L["X"], L["W"]), "DGRAD": (L["dY"], Wt), "WGRAD": (L["dYc"], L["Xc"])}
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile", [1, 2, 3])
 @pytest.mark.parametrize("M,K,N", [(128, 256, 512), (208, 192, 144), (320, 1024, 272),
                                    (128, 64, 16)])
-def test_gemm_small(nv, orc, M, K, N, tile_n):
+def test_gemm_small(nv, orc, M, K, N, tile):
     L = _layer(orc, M, K, N)
     for name, (a, b) in _gemms(orc, L).items():
         if a["cols"] % 64 or b["rows"] % 8:
             continue  # WGRAD of a ragged token count: K = M must be a multiple of 64
         A, B = H.upload(nv, a), H.upload(nv, b)
-        D = nv.nvfp4_gemm(A, B, tile_n=tile_n)
+        D = nv.nvfp4_gemm(A, B, tile=tile)
         nv.check_device_errors()
         H.assert_gemm_close(H.host_f64(D), orc.gemm_fp64(a, b), f"{name} {M}x{N}x{a['cols']}")
 
