@@ -146,6 +146,28 @@ nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64
                             uint64_t offset, nvfp4_tensor* out, void* workspace,
                             size_t workspace_bytes, nvfp4_stream stream);
 
+/* nvfp4_quantize without a workspace argument; the paper has no counterpart
+ * to this entry point.  It is for callers that cannot provide device scratch
+ * memory -- code running during CUDA graph capture (where cudaMalloc is not
+ * allowed), plugins given only input and output pointers, or programs whose
+ * allocator owns all device memory.  The per-CTA partial maxima of the amax
+ * pass go to a fixed 4 KB array (1024 floats) inside the library, held on
+ * every GPU that loads the library until the process exits.  The caller still
+ * passes x and the output buffers of `out`, exactly as for nvfp4_quantize, and
+ * gets the same results.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The call itself allocates and frees nothing.  All calls share the
+ * one array: calls that can overlap on the GPU (different streams, no
+ * ordering between them) race and must not be issued that way.  Each call's
+ * amax pass rewrites every partial its quantise pass reads, so nothing needs
+ * clearing between calls.  Returns NVFP4_ERR_WORKSPACE if the device has more
+ * SMs than the array can hold partials for (4 per SM, so above 256 SMs);
+ * otherwise the same statuses as nvfp4_quantize. */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                    int64_t ld, int32_t mode, uint32_t flags, uint64_t seed,
+                                    uint64_t offset, nvfp4_tensor* out, nvfp4_stream stream);
+
 /* ---------------------------------------------------------------------- */
 /* Block-scaled GEMM                                                       */
 /* ---------------------------------------------------------------------- */

@@ -62,6 +62,8 @@ def _load():
         "nvfp4_quantize_sizes": ([i64, i64, i32, u32, P(sz), P(sz), P(sz), P(sz)], C.c_int),
         "nvfp4_quantize": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp, sz, vp],
                            C.c_int),
+        "nvfp4_quantize_noalloc": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp],
+                                   C.c_int),
         "nvfp4_gemm": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, vp, sz, vp],
                        C.c_int),
         "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
@@ -180,6 +182,24 @@ def nvfp4_quantize(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0, of
                               C.byref(out.desc), _ptr(workspace),
                               0 if workspace is None else workspace.numel(), _stream(stream)),
            "nvfp4_quantize")
+    return out
+
+
+def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0,
+                           offset: int = 0, out: QTensor | None = None, stream=None) -> QTensor:
+    """nvfp4_quantize without a workspace: scratch lives inside the library
+    (see nvfp4_quantize_noalloc in nvfp4.h for who needs this and its limits)."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    dt = {torch.bfloat16: IN_BF16, torch.float32: IN_FP32}.get(x.dtype)
+    if dt is None:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    rows, cols = x.shape
+    if out is None:
+        out = alloc_qtensor(rows, cols, mode, flags, device=x.device)
+    _check(lib.nvfp4_quantize_noalloc(x.data_ptr(), dt, rows, cols, x.stride(0), mode, flags, seed,
+                                      offset, C.byref(out.desc), _stream(stream)),
+           "nvfp4_quantize_noalloc")
     return out
 
 

@@ -10,6 +10,7 @@
 // shared memory so every global store is a coalesced 4- or 16-byte store.
 // Kernels are persistent (grid-stride over tiles).
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -508,6 +509,69 @@ int64_t num_tiles(int mode, int64_t R, int64_t C) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// ---- entry point that allocates nothing ---------------------------------------
+// Some callers cannot hand the library a workspace: code that runs while a
+// CUDA graph is being captured (where cudaMalloc is not permitted), plugins
+// that receive only input and output pointers from a host framework, or
+// applications whose allocator owns all device memory.  For them the amax
+// partial maxima live in a fixed array inside the library instead.
+namespace {
+
+constexpr int kNoAllocPartials = kMaxPartials;  // 1024 floats: 4 KB per device
+// Lives on every device that loads the library, until the process exits.
+// In host code this name is only a stand-in: kernels receive the device
+// address obtained with cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of the array on the current device, looked up once per
+// device (the first call on a device does this; make that first call before
+// any stream capture).
+nvfp4_status noalloc_scratch(void** addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return NVFP4_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t in_dtype, int64_t rows,
+                                               int64_t cols, int64_t ld, int32_t mode,
+                                               uint32_t flags, uint64_t seed, uint64_t offset,
+                                               nvfp4_tensor* out, nvfp4_stream stream) {
+  using namespace nvfp4;
+  if (mode < NVFP4_ROW_1X16 || mode > NVFP4_BLOCK_16X16 || rows <= 0 || cols <= 0)
+    return nvfp4_quantize(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, out, nullptr, 0,
+                          stream);  // argument errors are reported as by nvfp4_quantize
+  if (flags & NVFP4_AMAX_GIVEN)      // no partial maxima needed
+    return quantize_impl(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, out, nullptr, 0,
+                         static_cast<cudaStream_t>(stream));
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  // the amax pass writes one partial per CTA: reject what the array cannot hold
+  if ((int64_t)dev.sm_count * 4 > kNoAllocPartials) return NVFP4_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != NVFP4_OK) return st;
+  // every partial the quantise pass reads is written by this call's amax pass
+  // first, so nothing needs clearing between calls
+  return quantize_impl(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, out, scratch,
+                       sizeof(float) * kNoAllocPartials, static_cast<cudaStream_t>(stream));
+}
+
+namespace nvfp4 {
 
 size_t swizzled_scale_bytes(int64_t rows, int64_t cols) {
   const int64_t prow = (rows + 127) / 128 * 128;
