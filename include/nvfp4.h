@@ -198,7 +198,9 @@ enum {
   NVFP4_TILE_AUTO = 0,          /* 128 x 256 on one SM (128 x 128 when N <= 128)           */
   NVFP4_TILE_128X128 = 1,       /* one SM per 128 x 128 tile                               */
   NVFP4_TILE_128X256 = 2,       /* one SM per 128 x 256 tile                               */
-  NVFP4_TILE_PAIR_256X256 = 3   /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */
+  NVFP4_TILE_PAIR_256X256 = 3,  /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */
+  NVFP4_TILE_128X256_MC2 = 4,   /* one SM per 128 x 256 tile, clusters of two sharing B    */
+  NVFP4_TILE_128X256_K128 = 5   /* one SM per 128 x 256 tile, 8 stages of K = 128          */
 };
 
 /* As nvfp4_gemm with an explicit output-tile configuration (NVFP4_TILE_*).

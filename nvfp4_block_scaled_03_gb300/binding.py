@@ -23,7 +23,8 @@ IN_BF16, IN_FP32 = 0, 1
 ROW_1X16, COL_1X16, BLOCK_16X16 = 0, 1, 2
 RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
 D_BF16, D_F32_ACCUM, D_BF16_ADD_C = 0, 1, 2
-TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256 = 0, 1, 2, 3
+TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256, TILE_128X256_MC2, TILE_128X256_K128 = \
+    0, 1, 2, 3, 4, 5
 
 
 class NVFP4Error(RuntimeError):

@@ -266,6 +266,34 @@ NVFP4_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t b
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
+// TMA tile load multicast to the same shared-memory offset (and mbarrier
+// offset) of every CTA in `mask`.
+NVFP4_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                              int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+// Arrive on the same-offset mbarrier of every CTA in `mask` when this thread's
+// prior tcgen05 operations complete (single-SM MMAs).
+NVFP4_DEV void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+// 5-D variant (coordinates 0, 0, 0, x3, x4) completing on a pair barrier.
+NVFP4_DEV void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                int32_t x3, int32_t x4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %3, %3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(0), "r"(x3), "r"(x4)
+      : "memory");
+}
 NVFP4_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -292,6 +320,21 @@ NVFP4_DEV void tc_commit_pair(uint32_t bar, uint16_t mask) {
 NVFP4_DEV void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
+}
+// 128 lanes x 256 bits in both CTAs: row L of each CTA's image (two 16-byte
+// chunks) to lane L, columns base .. base + 7.
+NVFP4_DEV void tc_cp_pair_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Descriptor of a 128-row x 32-byte image stored as two 2 KB chunk planes
+// (bytes 0-15 of row L at L * 16, bytes 16-31 at 2048 + L * 16); the copy
+// puts plane 0 in columns base .. base + 3 and plane 1 in base + 4 .. + 7.
+NVFP4_DEV uint64_t smem_desc_sf_image(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(2048 >> 4) << 16;  // leading byte offset: the second 16-byte chunk
+  d |= (uint64_t)(128 >> 4) << 32;   // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;
+  return d;
 }
 // Pair MMA: D (M = 256 split over the two CTAs' tensor memory) (+)= A . B^T.
 NVFP4_DEV void tc_mma_pair_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -33,7 +33,8 @@ static __device__ unsigned int g_gemm_error;
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps
+constexpr int kThreadsPair = 320;
 constexpr int kBM = 128;            // rows of A per tile (one MMA, cta_group::1)
 constexpr int kBKBytes = 128;       // K bytes per stage (256 FP4 elements)
 constexpr int kAtomsPerStage = 4;   // scale atoms per 128 rows per stage (K = 256)
@@ -51,14 +52,16 @@ struct GemmArgs {
   int num_m_blk;  // ceil(M / 128)
   int num_n_blk;  // ceil(N / BN)
   int nrb_b;      // 128-row blocks of B's scale tensor (ceil(N / 128))
+  int nrb_a;      // 128-row blocks of A's scale tensor (ceil(M / 128))
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int BKB>
 struct Smem {
-  static constexpr uint32_t kA = kBM * kBKBytes;                 // 16 KB
-  static constexpr uint32_t kB = BN * kBKBytes;                  // 16/32 KB
-  static constexpr uint32_t kSFA = kAtomsPerStage * 512;          // 2 KB
-  static constexpr uint32_t kSFB = (BN / 128) * kAtomsPerStage * 512;
+  static constexpr int kAtoms = BKB / 32;                        // scale atoms per 128 rows per stage
+  static constexpr uint32_t kA = kBM * BKB;                      // 16/8 KB
+  static constexpr uint32_t kB = BN * BKB;
+  static constexpr uint32_t kSFA = kAtoms * 512;
+  static constexpr uint32_t kSFB = (BN / 128) * kAtoms * 512;
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
   static constexpr uint32_t offSFA = offB + STAGES * kB;
@@ -70,10 +73,22 @@ struct Smem {
   static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024
   // tensor memory columns: accumulator [0, BN), then per-stage scales
   static constexpr uint32_t kSfCol0 = BN;
-  static constexpr uint32_t kSfColsPerStage = 16 + BN / 8;
+  static constexpr uint32_t kSfColsPerStage = (16 + BN / 8) * kAtoms / 4;
   static_assert(kSfCol0 + STAGES * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
   static_assert(kAlloc <= 232448, "shared memory overflow");
 };
+
+// K-major operand descriptor for a stage row width of BKB bytes (128-byte or
+// 64-byte swizzle; 8-row swizzle atoms stacked 8*BKB bytes apart).
+template <int BKB>
+NVFP4_DEV uint64_t smem_desc_kmajor(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)((8 * BKB) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(BKB == 128 ? 2 : 4) << 61;  // SWIZZLE_128B or SWIZZLE_64B
+  return d;
+}
 
 NVFP4_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                             unsigned int code) {
@@ -97,6 +112,25 @@ NVFP4_DEV void wait_drain(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
       atomicCAS(&g_gemm_error, 0u, 0xDEu);
       return;
+    }
+  }
+}
+
+// Bounded wait for a kernel launched in clusters of MC CTAs: a timeout also
+// raises the peer CTA's abort flag.
+template <int MC>
+NVFP4_DEV bool wait_bounded_mc(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                               uint32_t peer_abort_addr, unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      if (MC == 2) st_cluster_u32(peer_abort_addr, 1u);
+      atomicCAS(&g_gemm_error, 0u, code);
+      return false;
     }
   }
 }
@@ -153,11 +187,12 @@ NVFP4_DEV void store_row_chunk(const GemmArgs& a, int64_t row, int64_t col0, con
   }
 }
 
-template <int BN, int STAGES, int DMODE>
+template <int BN, int STAGES, int DMODE, int MC, int BKB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-  using L = Smem<BN, STAGES>;
+  using L = Smem<BN, STAGES, BKB>;
+  constexpr int kAt = L::kAtoms;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -172,13 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_kb = (args.K + 255) / 256;
-  const int num_tiles = args.num_m_blk * args.num_n_blk;
+  const int num_kb = (args.K + 2 * BKB - 1) / (2 * BKB);
+  // MC == 2: the two CTAs of a cluster take vertically adjacent tiles (same
+  // n_blk) and share their B tile -- each loads half and multicasts it.
+  const uint32_t rank = MC == 2 ? cluster_ctarank() : 0u;
+  const int num_mu = (args.num_m_blk + MC - 1) / MC;  // M units of MC tiles
+  const int num_units = num_mu * args.num_n_blk;
+  const int unit0 = blockIdx.x / MC, unit_step = gridDim.x / MC;
+  const uint32_t peer_abort =
+      MC == 2 ? mapa_shared(smem_u32(smem + L::offMisc + 4), rank ^ 1u) : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), MC);  // the MMA of every CTA that reads stage s
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -192,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (MC == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -204,26 +247,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       int armed[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+      for (int unit = unit0; ok && unit < num_units; unit += unit_step) {
+        const int m_blk = (unit % num_mu) * MC + (int)rank, n_blk = unit / num_mu;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, 0x10u)) { ok = false; break; }
-          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          if (!wait_bounded_mc<MC>(empty_bar(s), ph ^ 1u, abort_flag, peer_abort, 0x10u)) {
+            ok = false;
+            break;
+          }
+          const int natoms = min(kAt, args.kg - kb * kAt);
           int nb_valid = 0;
           for (int j = 0; j < BN / 128; ++j) nb_valid += (n_blk * (BN / 128) + j) < args.nrb_b;
           const uint32_t sf_bytes = (uint32_t)natoms * 512u * (1u + (uint32_t)nb_valid);
           mbar_arrive_expect_tx(full_bar(s), L::kA + L::kB + sf_bytes);
           armed[s] = (int)ph;
-          tma_load_2d(sbase + L::offA + s * L::kA, &tmA, full_bar(s), kb * kBKBytes, m_blk * kBM);
-          tma_load_2d(sbase + L::offB + s * L::kB, &tmB, full_bar(s), kb * kBKBytes, n_blk * BN);
+          tma_load_2d(sbase + L::offA + s * L::kA, &tmA, full_bar(s), kb * BKB, m_blk * kBM);
+          if (MC == 2)  // this CTA's half of the shared B tile, to both CTAs
+            tma_load_2d_mc(sbase + L::offB + s * L::kB + rank * (L::kB / 2), &tmB, full_bar(s),
+                           kb * BKB, n_blk * BN + (int)rank * (BN / 2), (uint16_t)3);
+          else
+            tma_load_2d(sbase + L::offB + s * L::kB, &tmB, full_bar(s), kb * BKB, n_blk * BN);
           bulk_load(sbase + L::offSFA + s * L::kSFA,
-                    args.sfa + ((int64_t)m_blk * args.kg + kb * kAtomsPerStage) * 512,
+                    args.sfa + ((int64_t)m_blk * args.kg + kb * kAt) * 512,
                     natoms * 512u, full_bar(s));
           for (int j = 0; j < BN / 128; ++j) {
             const int rb = n_blk * (BN / 128) + j;
             if (rb < args.nrb_b)
-              bulk_load(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512),
-                        args.sfb + ((int64_t)rb * args.kg + kb * kAtomsPerStage) * 512,
+              bulk_load(sbase + L::offSFB + s * L::kSFB + j * (kAt * 512),
+                        args.sfb + ((int64_t)rb * args.kg + kb * kAt) * 512,
                         natoms * 512u, full_bar(s));
           }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -240,13 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_nvf4(kBM, BN);
       uint32_t s = 0, ph = 0, acc_ph = 0;
       bool ok = true, issued = false;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        if (!wait_bounded(acc_empty, acc_ph ^ 1u, abort_flag, 0x20u)) { ok = false; break; }
+      for (int unit = unit0; ok && unit < num_units; unit += unit_step) {
+        if (!wait_bounded_mc<MC>(acc_empty, acc_ph ^ 1u, abort_flag, peer_abort, 0x20u)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(full_bar(s), ph, abort_flag, 0x21u)) { ok = false; break; }
+          if (!wait_bounded_mc<MC>(full_bar(s), ph, abort_flag, peer_abort, 0x21u)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const int natoms = min(kAt, args.kg - kb * kAt);
           const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 16;
           const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
@@ -260,12 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int b = 0; b < BN / 128; ++b)
               tc_cp_32x128b_warpx4(sfb_t + j * (BN / 32) + 4 * b,
-                                   smem_desc_sf(sb + b * (kAtomsPerStage * 512) + j * 512));
-            tc_mma_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j), idesc,
+                                   smem_desc_sf(sb + b * (kAt * 512) + j * 512));
+            tc_mma_nvf4(tmem, smem_desc_kmajor<BKB>(a0 + 32 * j), smem_desc_kmajor<BKB>(b0 + 32 * j), idesc,
                         sfa_t + 4 * j, sfb_t + j * (BN / 32), (kb | j) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit(empty_bar(s));
+          if (MC == 2) tc_commit_mc(empty_bar(s), 3);  // both CTAs wrote into this stage
+          else tc_commit(empty_bar(s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -286,9 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, h = (warp - 2) >> 2;
     const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
     uint32_t acc_ph = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
-      if (!wait_bounded(acc_full, acc_ph, abort_flag, 0x30u)) break;
+    for (int unit = unit0; unit < num_units; unit += unit_step) {
+      const int m_blk = (unit % num_mu) * MC + (int)rank, n_blk = unit / num_mu;
+      if (!wait_bounded_mc<MC>(acc_full, acc_ph, abort_flag, peer_abort, 0x30u)) break;
       tc_fence_after();
       uint32_t r[kChunks][32];
 #pragma unroll
@@ -310,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (MC == 2) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -325,8 +383,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // step's scales ahead of the MMA that reads them and commits to the empty /
 // accumulator barriers of both CTAs.  Each CTA's epilogue drains its 128
 // accumulator rows and releases them on the leader's barrier.  Per SM this
-// moves two thirds of the operand bytes of the single-CTA 128 x 256 tile for
-// the same MMA work, and issues half the scale copies per FLOP.
+// moves two thirds of the operand bytes of the single-CTA 128 x 256 tile and
+// reads half the B operand bytes from its own shared memory per MMA.
+//
+// A's scales reach tensor memory with two 128-lane x 256-bit copies per stage
+// instead of four replicating 32x128b.warpx4 copies: the TMA loads an 8 KB
+// image holding each of the stage's four scale atoms four times (row L of an
+// atom's plane is atom row L % 32; the replica dimension of the tensor map
+// has stride 0), so each copy puts two K steps' scales in tensor memory
+// exactly as the warpx4 copies would, at the same 4-aligned columns.  B's
+// scales keep the warpx4 copies.
 // =============================================================================
 constexpr int kPairBN = 256;
 
@@ -334,7 +400,7 @@ template <int STAGES>
 struct PairSmem {
   static constexpr uint32_t kA = 128 * kBKBytes;          // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;          // this CTA's 128 B rows
-  static constexpr uint32_t kSFA = kAtomsPerStage * 512;  // own A rows' scales
+  static constexpr uint32_t kSFA = 8192;  // replicated image of own A rows' scales
   static constexpr uint32_t kSFB = 2 * kAtomsPerStage * 512;  // the tile's 256 B rows' scales
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
@@ -347,7 +413,7 @@ struct PairSmem {
   static constexpr uint32_t kBytes = offMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kSfCol0 = kPairBN;
-  static constexpr uint32_t kSfColsPerStage = 16 + 32;
+  static constexpr uint32_t kSfColsPerStage = 16 + 32;  // A (4 K steps x 4), B (4 x 8)
   static_assert(kSfCol0 + STAGES * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
   static_assert(kAlloc <= 232448, "shared memory overflow");
 };
@@ -370,7 +436,7 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
 }
 
 template <int STAGES, int DMODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
@@ -441,9 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
           tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
                            (b_rb0 + (int)rank) * 128);
-          // scale atoms as 128-byte rows: 4 atoms = 16 rows per 128 operand rows
-          tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
-                           (a_rb * args.kg + kb * kAtomsPerStage) * 4);
+          // A's scale atoms, each replicated 4x (5-D map: byte, atom row,
+          // replica, atom along K, row block)
+          tma_load_5d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, kb * kAtomsPerStage, a_rb);
+          // B's scale atoms as 128-byte rows: 4 atoms = 16 rows per 128 B rows
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512), &tmSFB,
@@ -482,15 +549,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
           const uint32_t a0 = sbase + L::offA + s * L::kA;
           const uint32_t b0 = sbase + L::offB + s * L::kB;
-          auto copy_scales = [&](int j) {
-            tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
+          auto copy_b_scales = [&](int j) {
             tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j, smem_desc_sf(sb + j * 512));
             tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4,
                                       smem_desc_sf(sb + kAtomsPerStage * 512 + j * 512));
           };
-          copy_scales(0);
+          tc_cp_pair_128x256b(sfa_t, smem_desc_sf_image(sa));             // K steps 0, 1
+          if (natoms > 2) tc_cp_pair_128x256b(sfa_t + 8, smem_desc_sf_image(sa + 4096));  // 2, 3
+          copy_b_scales(0);
           for (int j = 0; j < natoms; ++j) {
-            if (j + 1 < natoms) copy_scales(j + 1);  // next step's scales ahead of this MMA
+            if (j + 1 < natoms) copy_b_scales(j + 1);  // next step's scales ahead of this MMA
             tc_mma_pair_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
                              idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
           }
@@ -565,17 +633,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over a K-major code matrix [rows, kbytes] with a 128-byte x box_rows box.
+// 2-D map over a K-major code matrix [rows, kbytes] with a box of box_bytes
+// (128: 128-byte swizzle, 64: 64-byte swizzle) x box_rows.
 bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes,
-                   int box_rows) {
+                   int box_rows, int box_bytes = kBKBytes) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
-  const cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
+  const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -593,6 +663,22 @@ bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes) {
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 5-D map over a scale tensor that replicates each 512-byte atom four times:
+// dims (16 bytes of an atom row, 32 atom rows, 4 replicas with stride 0,
+// kg atoms along K, row blocks); box = one stage (4 atoms) of one row block.
+bool make_sf_rep_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kg) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int64_t nrb = (rows + 127) / 128;
+  const cuuint64_t dims[5] = {16, 32, 4, (cuuint64_t)kg, (cuuint64_t)nrb};
+  const cuuint64_t strides[4] = {16, 0, 512, (cuuint64_t)(kg * 512)};
+  const cuuint32_t box[5] = {16, 32, 4, (cuuint32_t)kAtomsPerStage, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int STAGES, int DMODE>
@@ -613,7 +699,7 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   if (max_pairs == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsPair);
     cfg.dynamicSmemBytes = L::kAlloc;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -628,15 +714,15 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   }
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(ma, mb, msa, msb, a);
+  kern<<<grid, kThreadsPair, L::kAlloc, stream>>>(ma, mb, msa, msb, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int DMODE>
+template <int BN, int STAGES, int DMODE, int MC, int BKB>
 nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int sms,
                     cudaStream_t stream) {
-  using L = Smem<BN, STAGES>;
-  auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE>;
+  using L = Smem<BN, STAGES, BKB>;
+  auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE, MC, BKB>;
   static bool configured = false;  // attribute is per function; setting it twice is harmless
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
@@ -644,19 +730,38 @@ nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs
       return NVFP4_ERR_CUDA;
     configured = true;
   }
-  const int tiles = a.num_m_blk * a.num_n_blk;
-  const int grid = std::min(tiles, sms);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(ma, mb, a);
+  const int units = ((a.num_m_blk + MC - 1) / MC) * a.num_n_blk;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = MC;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(MC * (sms / MC));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / MC;
+    max_clusters = std::min(n, sms / MC);
+  }
+  cfg.gridDim = dim3(MC * std::min(units, max_clusters));
+  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, a) != cudaSuccess) return NVFP4_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int MC, int BKB>
 nvfp4_status launch_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& mb,
                          const GemmArgs& a, int sms, cudaStream_t s) {
   switch (d_mode) {
-    case NVFP4_D_BF16: return launch<BN, STAGES, NVFP4_D_BF16>(ma, mb, a, sms, s);
-    case NVFP4_D_F32_ACCUM: return launch<BN, STAGES, NVFP4_D_F32_ACCUM>(ma, mb, a, sms, s);
-    default: return launch<BN, STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, a, sms, s);
+    case NVFP4_D_BF16: return launch<BN, STAGES, NVFP4_D_BF16, MC, BKB>(ma, mb, a, sms, s);
+    case NVFP4_D_F32_ACCUM:
+      return launch<BN, STAGES, NVFP4_D_F32_ACCUM, MC, BKB>(ma, mb, a, sms, s);
+    default: return launch<BN, STAGES, NVFP4_D_BF16_ADD_C, MC, BKB>(ma, mb, a, sms, s);
   }
 }
 
@@ -692,7 +797,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   if (a_view < 0 || a_view > 1 || b_view < 0 || b_view > 1) return NVFP4_ERR_INVALID_ARG;
   if (d_mode < NVFP4_D_BF16 || d_mode > NVFP4_D_BF16_ADD_C) return NVFP4_ERR_INVALID_ARG;
   if (d_mode == NVFP4_D_BF16_ADD_C && !C) return NVFP4_ERR_INVALID_ARG;
-  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_PAIR_256X256) return NVFP4_ERR_INVALID_ARG;
+  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_128X256_K128) return NVFP4_ERR_INVALID_ARG;
   const void* a_codes = a_view ? A->codes_t : A->codes;
   const void* a_sf = a_view ? A->scales_t : A->scales;
   const void* b_codes = b_view ? B->codes_t : B->codes;
@@ -725,11 +830,12 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   a.K = (int)K;
   a.kg = (int)(K / 64);
   a.nrb_b = (int)((N + 127) / 128);
+  a.nrb_a = (int)((M + 127) / 128);
   CUtensorMap ma, mb;
   if (tile == NVFP4_TILE_PAIR_256X256) {
     CUtensorMap msa, msb;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
-        !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
+        !make_sf_rep_map(&msa, a_sf, M, K / 64) ||
         !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
       return NVFP4_ERR_CUDA;
     a.num_m_blk = (int)((M + 255) / 256);
@@ -737,12 +843,17 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, a, dev.sm_count, stream);
   }
   const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
-  if (!make_code_map(&ma, a_codes, M, K / 2, kBM) || !make_code_map(&mb, b_codes, N, K / 2, bn))
+  const int mc = tile == NVFP4_TILE_128X256_MC2 ? 2 : 1;
+  const int bkb = tile == NVFP4_TILE_128X256_K128 ? 64 : 128;  // stage K bytes per row
+  if (!make_code_map(&ma, a_codes, M, K / 2, kBM, bkb) ||
+      !make_code_map(&mb, b_codes, N, K / 2, bn / mc, bkb))
     return NVFP4_ERR_CUDA;
   a.num_m_blk = (int)((M + kBM - 1) / kBM);
   a.num_n_blk = (int)((N + bn - 1) / bn);
-  if (bn == 256) return launch_mode<256, 4>(d_mode, ma, mb, a, dev.sm_count, stream);
-  return launch_mode<128, 6>(d_mode, ma, mb, a, dev.sm_count, stream);
+  if (bkb == 64) return launch_mode<256, 8, 1, 64>(d_mode, ma, mb, a, dev.sm_count, stream);
+  if (mc == 2) return launch_mode<256, 4, 2, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
+  if (bn == 256) return launch_mode<256, 4, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
+  return launch_mode<128, 6, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
 }
 
 }  // namespace nvfp4

@@ -43,7 +43,7 @@ def _gemms(orc, L):
     return {"FPROP": (L["X"], L["W"]), "DGRAD": (L["dY"], Wt), "WGRAD": (L["dYc"], L["Xc"])}
 
 
-@pytest.mark.parametrize("tile", [1, 2, 3])
+@pytest.mark.parametrize("tile", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("M,K,N", [(128, 256, 512), (208, 192, 144), (320, 1024, 272),
                                    (128, 64, 16)])
 def test_gemm_small(nv, orc, M, K, N, tile):
