@@ -63,10 +63,12 @@ nvfp4_status nvfp4_device_check(int device) {
 nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NVFP4_ERR_CUDA;
-  unsigned int code = 0;
-  nvfp4_status st = gemm_read_error(&code);
+  unsigned int gcode = 0, qcode = 0;
+  nvfp4_status st = gemm_read_error(&gcode);
   if (st != NVFP4_OK) return st;
-  return code ? NVFP4_ERR_DEVICE_TIMEOUT : NVFP4_OK;
+  st = quant_read_error(&qcode);
+  if (st != NVFP4_OK) return st;
+  return (gcode || qcode) ? NVFP4_ERR_DEVICE_TIMEOUT : NVFP4_OK;
 }
 
 nvfp4_status nvfp4_quantize_sizes(int64_t rows, int64_t cols, int32_t mode, uint32_t flags,

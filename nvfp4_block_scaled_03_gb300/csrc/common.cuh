@@ -33,12 +33,38 @@ NVFP4_DEV uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
   return c;
 }
 
+// The twenty round keys of Philox4x32-10 for one 64-bit key (round i uses
+// key + i * Weyl constants): computed once on the host and read by the
+// kernels from their parameters, so a call costs only the ten S-box rounds.
+struct PhiloxKeys {
+  uint32_t k[20];
+};
+inline PhiloxKeys philox_round_keys(uint64_t seed) {
+  PhiloxKeys r;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    r.k[2 * i] = k0;
+    r.k[2 * i + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return r;
+}
+NVFP4_DEV uint4 philox4x32_10_rk(uint4 c, const PhiloxKeys& rk) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ rk.k[2 * round], lo1, hi0 ^ c.w ^ rk.k[2 * round + 1], lo0);
+  }
+  return c;
+}
+
 // Stochastic-rounding words for the 4 consecutive output elements starting at
 // linear index idx4 (a multiple of 4): counter (idx4/4, stream 0, offset).
-NVFP4_DEV uint4 sr_words(uint64_t seed, uint64_t offset, uint64_t idx4) {
+NVFP4_DEV uint4 sr_words(const PhiloxKeys& rk, uint64_t offset, uint64_t idx4) {
   const uint64_t g = idx4 >> 2;
-  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), 0u, (uint32_t)offset),
-                       (uint32_t)seed, (uint32_t)(seed >> 32));
+  return philox4x32_10_rk(make_uint4((uint32_t)g, (uint32_t)(g >> 32), 0u, (uint32_t)offset), rk);
 }
 
 // 16 RHT sign bits (bit i set -> sign -1): word 0 of counter (0, 0, 1, 0).
@@ -78,27 +104,38 @@ NVFP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 // Stochastic rounding of y onto the E2M1 grid {0,.5,1,1.5,2,3,4,6}: rounds
 // |y| up to the next grid value iff r < floor(frac * 2^32), frac =
 // (|y| - lo) / (hi - lo).  Returns the 4-bit code, sign kept; |y| >= 6
-// saturates.  Evaluated exactly on the float's bits: for |y| >= 1 the grid
-// keeps one mantissa bit, so frac * 2^32 is the 22 mantissa bits below it
-// shifted left by 10; on [0.5, 1) it is the 23 mantissa bits << 9; below 0.5
-// it is floor(|y| * 2^33) (an exact power-of-two scaling).
+// saturates.  Evaluated exactly and without branches on the float's bits:
+// for |y| >= 1 the grid keeps one mantissa bit and frac * 2^32 is the 22
+// bits below it shifted left by 10, so r < thr iff the 22-bit complement of
+// r's top 22 bits, added to those bits, carries into the kept bit -- adding
+// it to the whole word performs the round-up, binade changes included, and
+// the code is read off bits 22 and up.  On [0.5, 1) the same holds with 23
+// bits (the carry reaches the exponent); below 0.5 the threshold is
+// floor(|y| * 2^33), an exact power-of-two scaling.
 NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
   const uint32_t bits = __float_as_uint(y);
   const uint32_t sign = (bits >> 28) & 8u;
-  const uint32_t abits = bits & 0x7FFFFFFFu;
-  if (!(__uint_as_float(abits) < 6.0f)) return sign | 7u;
-  uint32_t code, thr;
-  if (abits >= 0x3F800000u) {  // [1, 6): binades [1,2), [2,4), [4,6)
-    code = ((((abits >> 23) - 127u) + 1u) << 1) | ((abits >> 22) & 1u);
-    thr = (abits & 0x3FFFFFu) << 10;
-  } else if (abits >= 0x3F000000u) {  // [0.5, 1)
-    code = 1u;
-    thr = (abits & 0x7FFFFFu) << 9;
-  } else {  // [0, 0.5)
-    code = 0u;
-    thr = __float2uint_rz(__fmul_rn(__uint_as_float(abits), 8589934592.0f));
-  }
-  return sign | (r < thr ? code + 1u : code);
+  const uint32_t a = bits & 0x7FFFFFFFu;
+  const bool ge1 = a >= 0x3F800000u;
+  const uint32_t t = a + ((~r) >> (ge1 ? 10 : 9));
+  const uint32_t code_hi = ge1 ? (t >> 22) - 252u : (t >> 23) - 125u;
+  const uint32_t thr = __float2uint_rz(__fmul_rn(__uint_as_float(a), 8589934592.0f));
+  uint32_t code = a < 0x3F000000u ? (thr > r ? 1u : 0u) : code_hi;
+  code = a < 0x40C00000u ? code : 7u;  // |y| >= 6 (or not finite) saturates
+  return sign | code;
+}
+
+// Correctly rounded a / 6 for a >= 2^-100 without a division: the product
+// with RN(1/6), one exact FMA residual and one FMA correction (Markstein's
+// correction step; correct rounding checked exhaustively over every binary32
+// finite a >= 2^-100).  Smaller a (subnormal quotients), infinities and NaN
+// take the IEEE division.
+NVFP4_DEV float div6_rn(float a) {
+  const float c = 0x1.555556p-3f;  // RN(1/6)
+  if (!(a >= 0x1p-100f && a <= 0x1.fffffep127f)) return __fdiv_rn(a, 6.0f);
+  const float q0 = __fmul_rn(a, c);
+  const float res = __fmaf_rn(-q0, 6.0f, a);
+  return __fmaf_rn(res, c, q0);
 }
 
 // Per-tensor encode scale from the amax: 6*448/amax, 1 for 0, FLT_MAX if the

@@ -2,6 +2,7 @@
 // units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -41,6 +42,17 @@ nvfp4_status swiglu_fwd_impl(const void* G, const void* U, void* H, int64_t n,
                              cudaStream_t stream);
 nvfp4_status swiglu_bwd_impl(const void* dH, const void* G, const void* U, void* dG, void* dU,
                              int64_t n, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry-point
+// query (null if the driver does not provide it).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
+// Reads and clears the quantisers' device error word (after a sync).
+nvfp4_status quant_read_error(unsigned int* code);
 
 inline nvfp4_status cuda_status(cudaError_t e) {
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;

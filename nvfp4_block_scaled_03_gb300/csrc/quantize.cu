@@ -4,11 +4,19 @@
 // stochastic rounding from Philox4x32-10) and writes the scales directly in
 // the MMA's 128x4 atom layout.
 //
-// All three modes are bandwidth kernels: 16-byte coalesced loads (8 elements
-// per thread), the 1x16 block amax with one warp shuffle (two threads per
-// block) or a register-resident block (column mode), and outputs staged in
-// shared memory so every global store is a coalesced 4- or 16-byte store.
-// Kernels are persistent (grid-stride over tiles).
+// The quantise pass is a persistent, warp-specialised kernel: one producer
+// thread streams input tiles into a ring of shared-memory stages with TMA
+// (boxes of 128-byte rows, 128-byte swizzle, zeros past the tensor's edges)
+// while eight consumer warps turn each stage into codes and scales.  A stage
+// is handed back as soon as its values sit in registers, so HBM reads run
+// ahead of the encoding.  Outputs leave through coalesced stores, staged in
+// shared memory per warp (or, for the transposing mode, per CTA behind a
+// bounded mbarrier).  The amax pre-pass is a plain bandwidth kernel with
+// wide loads and several loads in flight per thread.
+//
+// Every wait is bounded (2 s via %globaltimer): on expiry the kernel records
+// a code in the quantiser error word, raises its CTA's abort flag, the
+// producer waits (bounded) for the copies it issued and the CTA exits.
 #include <algorithm>
 #include <mutex>
 
@@ -17,15 +25,21 @@
 
 namespace nvfp4 {
 
+static __device__ unsigned int g_quant_error;
+
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kQThreads = kConsumers + 32;  // + one producer warp
+constexpr int kAmaxThreads = 256;
+constexpr uint64_t kQWaitNs = 2000000000ull;
 
 struct QParams {
-  const void* x;
   int64_t rows, cols, ld;  // input [rows, cols], leading dim in elements
   uint32_t flags;
   uint64_t seed, offset;
+  const void* x;           // amax pass only (the quantise pass reads through TMA)
   uint8_t* codes;
   uint8_t* scales;
   uint8_t* codes_t;
@@ -35,9 +49,111 @@ struct QParams {
   const float* amax_in;  // NVFP4_AMAX_GIVEN
   float* partials;       // amax pass: written; quantise pass: read
   int num_partials;
+  int codes_vec16;       // codes (and rows of codes) 16-byte aligned
+  int codes_t_vec8;      // transposed codes 8-byte aligned
+  PhiloxKeys rk;         // round keys of the stochastic-rounding generator (key = seed)
 };
 
-// ---- loads -----------------------------------------------------------------
+// ---- tile geometry -------------------------------------------------------------
+// A stage holds a tile of TR rows x TC columns of the input as NBOX TMA boxes
+// of TR rows x 128 bytes, each box 128-byte swizzled (the 16-byte chunk c of
+// row r sits at chunk c ^ (r % 8)), so row-wise and column-wise reads of the
+// stage are free of bank conflicts.
+template <typename T, int TR, int TC, int STAGES>
+struct Geo {
+  static constexpr int kTR = TR, kTC = TC, kStages = STAGES;
+  static constexpr int kBoxCols = 128 / (int)sizeof(T);
+  static constexpr int kNBox = TC / kBoxCols;
+  static constexpr uint32_t kBoxBytes = TR * 128;
+  static constexpr uint32_t kStageBytes = kNBox * kBoxBytes;
+  static_assert(TC % kBoxCols == 0 && TR % 8 == 0, "tile shape");
+};
+template <typename T>
+using RowGeo = Geo<T, 128, 64, sizeof(T) == 2 ? 4 : 3>;
+template <typename T>
+using ColGeo = Geo<T, 64, 128, sizeof(T) == 2 ? 4 : 3>;
+template <typename T>
+using BlkGeo = Geo<T, 128, 64, sizeof(T) == 2 ? 4 : 3>;
+
+// Shared memory: stages (1024-byte aligned for the swizzle), kernel-specific
+// staging, the encode table, reduction scratch, barriers, abort flag.
+template <class G, int EXTRA>
+struct QSmem {
+  static constexpr uint32_t offExtra = G::kStages * G::kStageBytes;
+  static constexpr uint32_t offTab = offExtra + EXTRA;
+  static constexpr uint32_t offRed = offTab + 512;
+  static constexpr uint32_t offBar = offRed + 64;  // full[S], empty[S], out[2]
+  static constexpr uint32_t offMisc = offBar + 8 * (2 * G::kStages + 2);
+  static constexpr uint32_t kBytes = offMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static_assert(EXTRA % 16 == 0, "staging alignment");
+};
+
+NVFP4_DEV uint8_t* align_smem_1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
+// Byte offset of (row r, byte b of the tile row) inside a stage.
+template <class G>
+NVFP4_DEV uint32_t swz(int r, int b) {
+  return (uint32_t)(b >> 7) * G::kBoxBytes + (uint32_t)r * 128u +
+         ((uint32_t)(((b >> 4) & 7) ^ (r & 7)) << 4) + (uint32_t)(b & 15);
+}
+
+// 8 consecutive elements starting at column c of row r.
+template <class G>
+NVFP4_DEV void lds8(const uint8_t* st, int r, int c, const uint16_t*, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(st + swz<G>(r, c * 2));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <class G>
+NVFP4_DEV void lds8(const uint8_t* st, int r, int c, const float*, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(st + swz<G>(r, c * 4));
+  const float4 b = *reinterpret_cast<const float4*>(st + swz<G>(r, c * 4 + 16));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// 2 consecutive elements starting at (even) column c of row r.
+template <class G>
+NVFP4_DEV float2 lds2(const uint8_t* st, int r, int c, const uint16_t*) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(st + swz<G>(r, c * 2));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <class G>
+NVFP4_DEV float2 lds2(const uint8_t* st, int r, int c, const float*) {
+  return *reinterpret_cast<const float2*>(st + swz<G>(r, c * 4));
+}
+
+// ---- bounded waits -------------------------------------------------------------
+NVFP4_DEV bool q_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kQWaitNs) {
+      *abort_flag = 1;
+      atomicCAS(&g_quant_error, 0u, code);
+      return false;
+    }
+  }
+}
+NVFP4_DEV void q_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kQWaitNs) {
+      atomicCAS(&g_quant_error, 0u, 0x4Fu);
+      return;
+    }
+  }
+}
+
+// ---- loads (amax pass) -----------------------------------------------------------
 NVFP4_DEV void load8(const uint16_t* p, float (&v)[8]) {
   const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -144,12 +260,21 @@ NVFP4_DEV void rht16_pair(float (&v)[8], uint32_t sign_bits, int half) {
 
 // ---- encode ------------------------------------------------------------------
 NVFP4_DEV uint32_t block_scale_code(float a_b, float s_enc) {
-  return e4m3_rn_satfinite(__fmul_rn(__fdiv_rn(a_b, 6.0f), s_enc));
+  return e4m3_rn_satfinite(__fmul_rn(div6_rn(a_b), s_enc));
 }
-NVFP4_DEV float encode_factor(uint32_t sc, float s_enc) {
-  const float S = e4m3_value(sc);
-  return S == 0.0f ? 0.0f : __fdiv_rn(s_enc, S);
+
+// Element encode factor s_enc / S for every scale byte a block can get
+// (block amaxes are non-negative, so bytes 0..127), 0 where S = 0: the same
+// binary32 quotient the per-block formula gives, divided once per CTA.
+constexpr int kEncTable = 128;
+NVFP4_DEV void fill_enc_table(float* tab, float s_enc) {
+  for (int i = threadIdx.x; i < kEncTable; i += blockDim.x) {
+    const float S = e4m3_value((uint32_t)i);
+    tab[i] = S == 0.0f ? 0.0f : __fdiv_rn(s_enc, S);
+  }
+  __syncthreads();
 }
+NVFP4_DEV float encode_factor(const float* tab, uint32_t sc) { return tab[sc & 127u]; }
 
 // 8 elements -> 32 bits of packed codes (element 0 in the lowest nibble).
 template <bool SR>
@@ -169,346 +294,645 @@ NVFP4_DEV uint32_t encode8(const float (&v)[8], float enc, uint4 w0, uint4 w1) {
   return out;
 }
 
-// =============================================================================
-// ROW_1X16: tile = 128 rows x 64 columns (one scale atom).  Thread t owns the
-// 8-element chunk (row t/8 + 32 i, columns 8 (t%8) ..) for i = 0..3; lanes
-// t and t^1 form a 16-element block.
-// =============================================================================
-template <typename T, bool RHT, bool SR, bool AMAX_ONLY>
-__global__ void __launch_bounds__(kThreads) quant_row_kernel(QParams p) {
-  __shared__ float red[kThreads / 32];
-  __shared__ __align__(16) uint8_t atom[512];
-  const int tid = threadIdx.x;
-  const int c8 = tid & 7, rsub = tid >> 3, half = c8 & 1;
-  const int64_t R = p.rows, C = p.cols;
-  const int64_t ntc = (C + 63) / 64, ntiles = ((R + 127) / 128) * ntc;
-  const int64_t atoms_per_row = ((C / 16) + 3) / 4;
-  const T* x = static_cast<const T*>(p.x);
-  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
-  float s_enc = 0.0f, my_max = 0.0f;
-  if (!AMAX_ONLY) s_enc = tensor_s_enc(p, red);
+// ---- shared-memory layouts of the three quantise kernels --------------------------
+constexpr int kColOutWords = 9;                             // 8 code words per output row + pad
+constexpr uint32_t kColOutBytes = 128 * kColOutWords * 4;   // staged codes of one tile
+constexpr uint32_t kColBuf = kColOutBytes + 512;            // + its scale atom
+constexpr int kBlkKWords = 9;                               // 8 code words per row + pad
+constexpr uint32_t kBlkWarpK = 16 * kBlkKWords * 4;         // K-major codes of a warp's 16 rows
+constexpr uint32_t kBlkWarpBytes = kBlkWarpK + 512;         // + transposed codes, 64 x 8 bytes
+template <typename T>
+using RowL = QSmem<RowGeo<T>, kConsumerWarps * 64>;
+template <typename T>
+using ColL = QSmem<ColGeo<T>, 2 * kColBuf>;
+template <typename T>
+using BlkL = QSmem<BlkGeo<T>, kConsumerWarps * kBlkWarpBytes>;
 
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t tr = tile / ntc, tc = tile % ntc;
-    const int64_t c0 = tc * 64 + c8 * 8;
+// ---- pipeline pieces shared by the quantise kernels ----------------------------
+// Barriers: full[s] (count 1, completed by the TMA bytes), empty[s] (one
+// arrive per consumer warp), out[2] (one arrive per consumer warp; used by the
+// transposing kernel to hand its staged tile to the storing warps).
+template <class G, class L>
+NVFP4_DEV void q_init(uint8_t* smem) {
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_u32(smem + L::offBar);
+    for (int s = 0; s < G::kStages; ++s) {
+      mbar_init(bar + 8 * s, 1);
+      mbar_init(bar + 8 * (G::kStages + s), kConsumerWarps);
+    }
+    mbar_init(bar + 8 * (2 * G::kStages), kConsumerWarps);
+    mbar_init(bar + 8 * (2 * G::kStages + 1), kConsumerWarps);
+    *reinterpret_cast<volatile int*>(smem + L::offMisc) = 0;
+    fence_mbar_init();
+  }
+}
+
+// Producer (one thread): the CTA's tiles in order, tile = blockIdx.x +
+// k * gridDim.x into stage k % S.
+template <class G>
+NVFP4_DEV void q_produce(const CUtensorMap* tm, uint32_t stage0, uint32_t bar_full,
+                         uint32_t bar_empty, volatile int* abort_flag, int64_t ntiles,
+                         int64_t ntc) {
+  prefetch_tmap(tm);
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % G::kStages);
+    if (!q_wait(bar_empty + 8 * s, (uint32_t)((k / G::kStages) & 1) ^ 1u, abort_flag, 0x40u))
+      break;
+    const int32_t x = (int32_t)((tile % ntc) * G::kTC), y = (int32_t)((tile / ntc) * G::kTR);
+    mbar_arrive_expect_tx(bar_full + 8 * s, G::kStageBytes);
+#pragma unroll
+    for (int b = 0; b < G::kNBox; ++b)
+      tma_load_2d(stage0 + s * G::kStageBytes + b * G::kBoxBytes, tm, bar_full + 8 * s,
+                  x + b * G::kBoxCols, y);
+  }
+  // wait for the last copy issued into each stage: none is in flight at exit
+  for (int s = 0; s < G::kStages && s < k; ++s) {
+    const int64_t kl = s + G::kStages * ((k - 1 - s) / G::kStages);
+    q_drain(bar_full + 8 * s, (uint32_t)((kl / G::kStages) & 1));
+  }
+}
+
+// =============================================================================
+// ROW_1X16: tile = 128 rows x 64 columns (one scale atom).  Consumer thread t
+// owns the 8-element chunk (row t/8 + 32 i, columns 8 (t%8) ..) for i = 0..3;
+// lanes t and t^1 form a 16-element block.  Warp w's rows are 4w..4w+3 (+32 i),
+// which is exactly bytes 64w..64w+63 of the tile's scale atom, so each warp
+// writes its codes and its slice of the atom without waiting for the others.
+// =============================================================================
+template <typename T, bool RHT, bool SR>
+__global__ void __launch_bounds__(kQThreads, 2)
+    quant_row_kernel(const __grid_constant__ CUtensorMap tm, const QParams p) {
+  using G = RowGeo<T>;
+  using L = RowL<T>;
+  extern __shared__ uint8_t q_smem_raw[];
+  uint8_t* smem = align_smem_1024(q_smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar_full = smem_u32(smem + L::offBar);
+  const uint32_t bar_empty = bar_full + 8 * G::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
+  float* tab = reinterpret_cast<float*>(smem + L::offTab);
+  q_init<G, L>(smem);
+  const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
+  fill_enc_table(tab, s_enc);  // ends with a CTA barrier
+
+  const int64_t R = p.rows, C = p.cols;
+  const int64_t ntc = (C + G::kTC - 1) / G::kTC, ntiles = ((R + G::kTR - 1) / G::kTR) * ntc;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) q_produce<G>(&tm, smem_u32(smem), bar_full, bar_empty, abort_flag, ntiles, ntc);
+    return;
+  }
+  const int c8 = tid & 7, rsub = tid >> 3, half = c8 & 1;
+  const int64_t apr = ((C / 16) + 3) / 4;
+  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
+  uint8_t* wat = smem + L::offExtra + warp * 64;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % G::kStages);
+    if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
+    const uint8_t* st = smem + s * G::kStageBytes;
     float v[4][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = tr * 128 + i * 32 + rsub;
-      if (r < R && c0 < C) {
-        load8(x + r * p.ld + c0, v[i]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
-      }
-    }
+    for (int i = 0; i < 4; ++i)
+      lds8<G>(st, rsub + 32 * i, c8 * 8, static_cast<const T*>(nullptr), v[i]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+
+    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t c0 = tc * G::kTC + c8 * 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int64_t r = tr * 128 + i * 32 + rsub;
+      const int64_t r = tr * G::kTR + i * 32 + rsub;
       const bool ok = r < R && c0 < C;
       if (RHT) rht16_pair(v[i], sign_bits, half);
       float m = 0.0f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[i][e]));
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      if (AMAX_ONLY) {
-        my_max = fmaxf(my_max, m);
-        continue;
-      }
       const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
-      const float enc = encode_factor(sc, s_enc);
+      const float enc = encode_factor(tab, sc);
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
       if (SR && ok) {
         const uint64_t idx = (uint64_t)(r * C + c0);
-        w0 = sr_words(p.seed, p.offset, idx);
-        w1 = sr_words(p.seed, p.offset, idx + 4);
+        w0 = sr_words(p.rk, p.offset, idx);
+        w1 = sr_words(p.rk, p.offset, idx + 4);
       }
       const uint32_t packed = encode8<SR>(v[i], enc, w0, w1);
       if (ok) *reinterpret_cast<uint32_t*>(p.codes + r * (C / 2) + c0 / 2) = packed;
-      if (half == 0) atom[rsub * 16 + i * 4 + (c8 >> 1)] = (uint8_t)sc;
+      if (half == 0) wat[(rsub & 3) * 16 + i * 4 + (c8 >> 1)] = (uint8_t)sc;
     }
-    if (!AMAX_ONLY) {
-      __syncthreads();
-      if (tid < 32)
-        reinterpret_cast<uint4*>(p.scales + (tr * atoms_per_row + tc) * 512)[tid] =
-            reinterpret_cast<const uint4*>(atom)[tid];
-      __syncthreads();
-    }
+    __syncwarp();
+    if (lane < 4)
+      reinterpret_cast<uint4*>(p.scales + (tr * apr + tc) * 512 + warp * 64)[lane] =
+          reinterpret_cast<const uint4*>(wat)[lane];
+    __syncwarp();
   }
-  if (AMAX_ONLY) {
-    const float m = block_max(my_max, red);
-    if (tid == 0) p.partials[blockIdx.x] = m;
+}
+
+// One output row (input column c0 + ol) of a COL_1X16 tile: 16 values of the
+// 16-row block j -> RHT, scale, codes, staged for the coalesced store.
+template <bool RHT, bool SR>
+NVFP4_DEV void col_block(float (&v)[16], int ol, int j, bool rows_ok, int64_t c0, int64_t r0,
+                         int64_t R, int64_t C, float s_enc, const float* tab, uint32_t sign_bits,
+                         const QParams& p, uint32_t* out_s, uint8_t* atom) {
+  const int64_t col = c0 + ol;
+  const bool ok = rows_ok && col < C;
+  if (RHT) rht16_block(v, sign_bits);
+  float m = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+  const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
+  const float enc = encode_factor(tab, sc);
+  uint4 w[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                make_uint4(0, 0, 0, 0)};
+  if (SR && ok) {
+    const uint64_t idx = (uint64_t)(col * R + r0 + 16 * j);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = sr_words(p.rk, p.offset, idx + 4 * q);
   }
+  float lo[8], hi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    lo[e] = v[e];
+    hi[e] = v[8 + e];
+  }
+  out_s[ol * kColOutWords + 2 * j] = encode8<SR>(lo, enc, w[0], w[1]);
+  out_s[ol * kColOutWords + 2 * j + 1] = encode8<SR>(hi, enc, w[2], w[3]);
+  atom[(ol & 31) * 16 + ((ol >> 5) & 3) * 4 + j] = (uint8_t)sc;
 }
 
 // =============================================================================
 // COL_1X16 (transposing): tile = 64 input rows x 128 input columns, i.e. an
-// output tile of 128 rows x 64 columns -- one scale atom.  Loaded coalesced
-// into shared memory, then each thread quantises one 16-element column block
-// (output row c, 16 consecutive input rows) from registers: RHT butterfly,
-// block amax, scale, codes.  Codes and the atom are staged and written out
-// as coalesced rows.
+// output tile of 128 rows x 64 columns -- one scale atom.  Consumer warp w,
+// lane l owns the column pair 2 (l + 32 (w % 2)), +1 and the 16-row block
+// w / 2: 16 conflict-free 4- or 8-byte reads of the stage, then per column the
+// RHT butterfly, block amax, scale and codes from registers.  Codes and the
+// atom are staged in shared memory (double-buffered) and, after every warp
+// has arrived on the out barrier, written out as coalesced rows.
 // =============================================================================
-constexpr int kColTileR = 64, kColTileC = 128, kColPad = 132;
+template <typename T, bool RHT, bool SR>
+__global__ void __launch_bounds__(kQThreads, 2)
+    quant_col_kernel(const __grid_constant__ CUtensorMap tm, const QParams p) {
+  using G = ColGeo<T>;
+  using L = ColL<T>;
+  constexpr int kOutWords = kColOutWords;
+  constexpr uint32_t kOutBytes = kColOutBytes, kBuf = kColBuf;
+  extern __shared__ uint8_t q_smem_raw[];
+  uint8_t* smem = align_smem_1024(q_smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar_full = smem_u32(smem + L::offBar);
+  const uint32_t bar_empty = bar_full + 8 * G::kStages;
+  const uint32_t bar_out = bar_full + 16 * G::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
+  float* tab = reinterpret_cast<float*>(smem + L::offTab);
+  q_init<G, L>(smem);
+  const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
+  fill_enc_table(tab, s_enc);
 
-template <typename T, bool RHT, bool SR, bool AMAX_ONLY>
-__global__ void __launch_bounds__(kThreads) quant_col_kernel(QParams p) {
-  __shared__ __align__(16) float tile_s[kColTileR][kColPad];
-  __shared__ __align__(16) uint32_t out_s[kColTileC][9];  // 32 code bytes per row, padded
-  __shared__ __align__(16) uint8_t atom[512];
-  __shared__ float red[kThreads / 32];
-  const int tid = threadIdx.x;
   const int64_t R = p.rows, C = p.cols;  // output is [C, R]
-  const int64_t ntc = (C + kColTileC - 1) / kColTileC;
-  const int64_t ntiles = ((R + kColTileR - 1) / kColTileR) * ntc;
-  const int64_t atoms_per_row = ((R / 16) + 3) / 4;
-  const T* x = static_cast<const T*>(p.x);
-  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
-  float s_enc = 0.0f, my_max = 0.0f;
-  if (!AMAX_ONLY) s_enc = tensor_s_enc(p, red);
-
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t tr = tile / ntc, tc = tile % ntc;
-    const int64_t r0 = tr * kColTileR, c0 = tc * kColTileC;
-    // load phase: thread -> (row tid/16 + 16 i, chunk tid%16)
-    {
-      const int ch = tid & 15;
-      float v[4][8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rl = (tid >> 4) + 16 * i;
-        const int64_t r = r0 + rl, c = c0 + ch * 8;
-        if (r < R && c < C) {
-          load8(x + r * p.ld + c, v[i]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rl = (tid >> 4) + 16 * i;
-        float4* dst = reinterpret_cast<float4*>(&tile_s[rl][ch * 8]);
-        dst[0] = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
-        dst[1] = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
-      }
-    }
-    __syncthreads();
-    // compute phase: thread -> (output row c = tid % 128, block j)
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int cl = tid & 127, j = (tid >> 7) + 2 * it;
-      const bool ok = (c0 + cl < C) && (r0 + 16 * j < R);
-      float v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = tile_s[16 * j + e][cl];
-      if (RHT) rht16_block(v, sign_bits);
-      float m = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
-      if (AMAX_ONLY) {
-        my_max = fmaxf(my_max, m);
-        continue;
-      }
-      const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
-      const float enc = encode_factor(sc, s_enc);
-      uint4 w[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                    make_uint4(0, 0, 0, 0)};
-      if (SR && ok) {
-        const uint64_t idx = (uint64_t)((c0 + cl) * R + r0 + 16 * j);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) w[q] = sr_words(p.seed, p.offset, idx + 4 * q);
-      }
-      float lo[8], hi[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        lo[e] = v[e];
-        hi[e] = v[8 + e];
-      }
-      out_s[cl][2 * j] = encode8<SR>(lo, enc, w[0], w[1]);
-      out_s[cl][2 * j + 1] = encode8<SR>(hi, enc, w[2], w[3]);
-      atom[(cl & 31) * 16 + ((cl >> 5) & 3) * 4 + j] = (uint8_t)sc;
-    }
-    if (!AMAX_ONLY) {
-      __syncthreads();
-      // codes: 128 output rows x 8 words
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int wi = tid + kThreads * k;
-        const int rl = wi >> 3, word = wi & 7;
-        const int64_t orow = c0 + rl;
-        if (orow < C && r0 + word * 8 < R)
-          *reinterpret_cast<uint32_t*>(p.codes + orow * (R / 2) + r0 / 2 + word * 4) =
-              out_s[rl][word];
-      }
-      if (tid < 32)
-        reinterpret_cast<uint4*>(p.scales + (tc * atoms_per_row + tr) * 512)[tid] =
-            reinterpret_cast<const uint4*>(atom)[tid];
-    }
-    __syncthreads();
+  const int64_t ntc = (C + G::kTC - 1) / G::kTC, ntiles = ((R + G::kTR - 1) / G::kTR) * ntc;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) q_produce<G>(&tm, smem_u32(smem), bar_full, bar_empty, abort_flag, ntiles, ntc);
+    return;
   }
-  if (AMAX_ONLY) {
-    const float m = block_max(my_max, red);
-    if (tid == 0) p.partials[blockIdx.x] = m;
+  const int cp = lane + 32 * (warp & 1), j = warp >> 1;
+  const int64_t apr = ((R / 16) + 3) / 4;
+  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % G::kStages);
+    if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
+    const uint8_t* st = smem + s * G::kStageBytes;
+    float va[16], vb[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float2 f = lds2<G>(st, 16 * j + e, 2 * cp, static_cast<const T*>(nullptr));
+      va[e] = f.x;
+      vb[e] = f.y;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+
+    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
+    const int buf = (int)(k & 1);
+    uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
+    uint8_t* atom = smem + L::offExtra + buf * kBuf + kOutBytes;
+    const bool rows_ok = r0 + 16 * j < R;
+    col_block<RHT, SR>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p, out_s, atom);
+    col_block<RHT, SR>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p, out_s,
+                       atom);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_out + 8 * buf);
+    if (!q_wait(bar_out + 8 * buf, (uint32_t)((k >> 1) & 1), abort_flag, 0x42u)) break;
+    // warp w stores output rows 16w..16w+15: lane -> row 16w + lane/2, words 4 (lane%2) ..
+    const int orl = 16 * warp + (lane >> 1), wq = (lane & 1) * 4;
+    const int64_t orow = c0 + orl;
+    if (orow < C) {
+      uint8_t* dst = p.codes + orow * (R / 2) + r0 / 2 + wq * 4;
+      const uint32_t* src = out_s + orl * kOutWords + wq;
+      if (p.codes_vec16 && r0 + 8 * (wq + 4) <= R) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (r0 + 8 * (wq + q) < R) reinterpret_cast<uint32_t*>(dst)[q] = src[q];
+      }
+    }
+    if (warp == 0)
+      reinterpret_cast<uint4*>(p.scales + (tc * apr + tr) * 512)[lane] =
+          reinterpret_cast<const uint4*>(atom)[lane];
   }
 }
 
 // =============================================================================
-// BLOCK_16X16 (weights): tile = 128 x 128 elements = 8 x 8 scale tiles.  Warp
-// w owns rows 16w..16w+15; lane -> (row lane/2, half lane%2), 8 elements per
-// 16x16 tile.  One warp reduction gives the tile amax.  Writes the K-major
-// codes and, with EMIT_T, the nibble-transposed codes built from the same
-// codes (the partner row's codes arrive by one shuffle), plus both scale
-// layouts.
+// BLOCK_16X16 (weights): tile = 128 rows x 64 columns = 8 x 4 scale tiles.
+// Consumer warp w owns rows 16w..16w+15; lane -> (row lane % 16, half lane /
+// 16), 8 elements of each of the 4 16x16 tiles, whose amax is one warp
+// reduction.  Writes the K-major codes and, with EMIT_T, the nibble-transposed
+// codes built from the same codes (the partner row's codes arrive by one
+// shuffle), plus both scale layouts.  Every output of warp w comes from its
+// own 16 rows, so warps never wait for each other.
 // =============================================================================
 template <typename T, bool SR, bool EMIT_T>
-__global__ void __launch_bounds__(kThreads) quant_16x16_kernel(QParams p) {
-  __shared__ __align__(16) uint32_t outk_s[128][17];  // 64 code bytes per row, padded
-  __shared__ __align__(16) uint8_t outt_s[128][68];
-  __shared__ __align__(16) uint8_t atoms_k[2][512];
-  __shared__ __align__(16) uint8_t atoms_t[2][512];
-  __shared__ float red[kThreads / 32];
+__global__ void __launch_bounds__(kQThreads, 2)
+    quant_16x16_kernel(const __grid_constant__ CUtensorMap tm, const QParams p) {
+  using G = BlkGeo<T>;
+  using L = BlkL<T>;
+  constexpr int kKWords = kBlkKWords;
+  constexpr uint32_t kWarpK = kBlkWarpK, kWarpBytes = kBlkWarpBytes;
+  extern __shared__ uint8_t q_smem_raw[];
+  uint8_t* smem = align_smem_1024(q_smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nl = lane >> 1, half = lane & 1;
+  const uint32_t bar_full = smem_u32(smem + L::offBar);
+  const uint32_t bar_empty = bar_full + 8 * G::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
+  float* tab = reinterpret_cast<float*>(smem + L::offTab);
+  q_init<G, L>(smem);
+  const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
+  fill_enc_table(tab, s_enc);
+
   const int64_t R = p.rows, C = p.cols;
-  const int64_t ntc = (C + 127) / 128, ntiles = ((R + 127) / 128) * ntc;
+  const int64_t ntc = (C + G::kTC - 1) / G::kTC, ntiles = ((R + G::kTR - 1) / G::kTR) * ntc;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) q_produce<G>(&tm, smem_u32(smem), bar_full, bar_empty, abort_flag, ntiles, ntc);
+    return;
+  }
+  const int rl16 = lane & 15, h = lane >> 4;
+  const int rl = 16 * warp + rl16;
   const int64_t apr_k = ((C / 16) + 3) / 4;  // atoms per 128-row block, K-major view
   const int64_t apr_t = ((R / 16) + 3) / 4;  // transposed view
-  const T* x = static_cast<const T*>(p.x);
-  const float s_enc = tensor_s_enc(p, red);
+  uint32_t* ok_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + warp * kWarpBytes);
+  uint8_t* ot_s = smem + L::offExtra + warp * kWarpBytes + kWarpK;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % G::kStages);
+    if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
+    const uint8_t* st = smem + s * G::kStageBytes;
+    float v[4][8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      lds8<G>(st, rl, 16 * b + 8 * h, static_cast<const T*>(nullptr), v[b]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
 
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t tr = tile / ntc, tc = tile % ntc;
-    const int64_t r0 = tr * 128, c0 = tc * 128;
-    const int rl = warp * 16 + nl;
+    const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
     const int64_t r = r0 + rl;
-    const bool row_ok = r0 + warp * 16 < R;  // rows come in whole 16-row strips
-    float v[8][8];
+    const bool row_ok = r0 + 16 * warp < R;  // rows come in whole 16-row strips
+    const int64_t g = tr * 8 + warp;         // 16-row block: scale column of the transposed view
+    uint32_t scw = 0;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int64_t c = c0 + t * 16 + half * 8;
-      if (row_ok && c < C) {
-        load8(x + r * p.ld + c, v[t]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[t][e] = 0.0f;
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int64_t c = c0 + t * 16 + half * 8;
-      const bool ok = row_ok && (c0 + t * 16 < C);
+    for (int b = 0; b < 4; ++b) {
+      const bool ok = row_ok && (c0 + 16 * b < C);
       float m = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[t][e]));
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[b][e]));
       m = warp_max(m);
       const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
-      const float enc = encode_factor(sc, s_enc);
+      const float enc = encode_factor(tab, sc);
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
       if (SR && ok) {
-        const uint64_t idx = (uint64_t)(r * C + c);
-        w0 = sr_words(p.seed, p.offset, idx);
-        w1 = sr_words(p.seed, p.offset, idx + 4);
+        const uint64_t idx = (uint64_t)(r * C + c0 + 16 * b + 8 * h);
+        w0 = sr_words(p.rk, p.offset, idx);
+        w1 = sr_words(p.rk, p.offset, idx + 4);
       }
-      const uint32_t packed = encode8<SR>(v[t], enc, w0, w1);
-      outk_s[rl][t * 2 + half] = packed;
+      const uint32_t packed = encode8<SR>(v[b], enc, w0, w1);
+      ok_s[rl16 * kKWords + 2 * b + h] = packed;
+      scw |= sc << (8 * b);
       if (EMIT_T) {
-        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, packed, 2);  // row rl ^ 1
-        if ((nl & 1) == 0) {
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, packed, 1);  // row rl ^ 1
+        if ((lane & 1) == 0) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t b = ((packed >> (4 * e)) & 0xFu) | (((other >> (4 * e)) & 0xFu) << 4);
-            outt_s[t * 16 + half * 8 + e][rl >> 1] = (uint8_t)b;
+          for (int e = 0; e < 8; ++e)
+            ot_s[(16 * b + 8 * h + e) * 8 + (rl16 >> 1)] =
+                (uint8_t)(((packed >> (4 * e)) & 0xFu) | (((other >> (4 * e)) & 0xFu) << 4));
+        }
+        // transposed scale of output row c0 + 16 b + lane, scale column g
+        if (lane < 16 && g < 4 * apr_t) {
+          const int64_t orow = c0 + 16 * b + lane;
+          p.scales_t[((orow >> 7) * apr_t + (g >> 2)) * 512 + (orow & 31) * 16 +
+                     ((orow >> 5) & 3) * 4 + (g & 3)] = (uint8_t)sc;
+        }
+      }
+    }
+    // K-major scales: the 4 bytes of row rl form one word of the tile's atom
+    if (h == 0)
+      *reinterpret_cast<uint32_t*>(p.scales + (tr * apr_k + tc) * 512 + (rl & 31) * 16 +
+                                   ((rl >> 5) & 3) * 4) = scw;
+    // the transposed view's scale rows past the last 64-column tile, up to the
+    // 128-row padding, belong to no tile: the CTA of that last tile zeroes them
+    if (EMIT_T && (tc & 1) == 0 && tc == ntc - 1 && g < 4 * apr_t) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int64_t orow = c0 + 64 + lane + 32 * q;
+        p.scales_t[((orow >> 7) * apr_t + (g >> 2)) * 512 + (orow & 31) * 16 +
+                   ((orow >> 5) & 3) * 4 + (g & 3)] = 0;
+      }
+    }
+    __syncwarp();
+    {  // K-major codes: lane -> row 16 w + lane / 2, 16 bytes (32 columns) lane % 2
+      const int rr = lane >> 1, hh = lane & 1;
+      const int64_t row = r0 + 16 * warp + rr, col = c0 + 32 * hh;
+      if (row < R && col < C) {
+        uint8_t* dst = p.codes + row * (C / 2) + col / 2;
+        const uint32_t* src = ok_s + rr * kKWords + 4 * hh;
+        if (p.codes_vec16 && col + 32 <= C) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (col + 8 * q < C) reinterpret_cast<uint32_t*>(dst)[q] = src[q];
+        }
+      }
+    }
+    if (EMIT_T && row_ok) {  // transposed codes: output rows c0 + lane (+32), 8 bytes each
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = lane + 32 * q;
+        if (c0 + c < C) {
+          uint8_t* dst = p.codes_t + (c0 + c) * (R / 2) + (r0 + 16 * warp) / 2;
+          const uint2 val = *reinterpret_cast<const uint2*>(ot_s + c * 8);
+          if (p.codes_t_vec8) {
+            *reinterpret_cast<uint2*>(dst) = val;
+          } else {
+            reinterpret_cast<uint32_t*>(dst)[0] = val.x;
+            reinterpret_cast<uint32_t*>(dst)[1] = val.y;
           }
         }
       }
-      // scale bytes: K-major rows rl (scale column t), transposed rows t*16+e
-      if (half == 0)
-        atoms_k[t >> 2][(rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (t & 3)] = (uint8_t)sc;
-      if (EMIT_T && lane < 16) {
-        const int kr = t * 16 + lane;
-        atoms_t[warp >> 2][(kr & 31) * 16 + ((kr >> 5) & 3) * 4 + (warp & 3)] = (uint8_t)sc;
-      }
     }
-    __syncthreads();
-    // K-major codes: 128 rows x 16 words
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int wi = tid + kThreads * k;
-      const int row = wi >> 4, word = wi & 15;
-      if (r0 + row < R && c0 + word * 8 < C)
-        *reinterpret_cast<uint32_t*>(p.codes + (r0 + row) * (C / 2) + c0 / 2 + word * 4) =
-            outk_s[row][word];
-    }
-    if (EMIT_T) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int wi = tid + kThreads * k;
-        const int row = wi >> 4, word = wi & 15;
-        if (c0 + row < C && r0 + word * 8 < R)
-          *reinterpret_cast<uint32_t*>(p.codes_t + (c0 + row) * (R / 2) + r0 / 2 + word * 4) =
-              *reinterpret_cast<const uint32_t*>(&outt_s[row][word * 4]);
-      }
-    }
-    if (tid < 64) {
-      const int a = tid >> 5, l = tid & 31;
-      const int64_t g = tc * 2 + a;  // scale-column group of the K-major view
-      if (g < apr_k)
-        reinterpret_cast<uint4*>(p.scales + (tr * apr_k + g) * 512)[l] =
-            reinterpret_cast<const uint4*>(atoms_k[a])[l];
-    } else if (EMIT_T && tid < 128) {
-      const int a = (tid - 64) >> 5, l = tid & 31;
-      const int64_t g = tr * 2 + a;  // scale-column group of the transposed view
-      if (g < apr_t)
-        reinterpret_cast<uint4*>(p.scales_t + (tc * apr_t + g) * 512)[l] =
-            reinterpret_cast<const uint4*>(atoms_t[a])[l];
-    }
-    __syncthreads();
+    __syncwarp();
   }
+}
+
+// =============================================================================
+// Amax pre-pass: per-CTA partial maxima of |x| (or of |RHT(x)| along the
+// dimension the quantiser transforms), written to the workspace.
+// =============================================================================
+// max |x|: 8-element chunks, four 16-byte loads in flight per thread.
+template <typename T>
+__global__ void __launch_bounds__(kAmaxThreads) amax_plain_kernel(const QParams p) {
+  __shared__ float red[kAmaxThreads / 32];
+  const T* x = static_cast<const T*>(p.x);
+  const int64_t C = p.cols, ld = p.ld, cpr = C / 8, n = p.rows * cpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += 4 * stride) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t q = i + u * stride;
+      if (q < n) {
+        const int64_t r = ld == C ? 0 : q / cpr;
+        const int64_t off = ld == C ? q * 8 : r * ld + (q - r * cpr) * 8;
+        load8(x + off, v[u]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+}
+
+// max |RHT(x)| with the transform along columns (16-row blocks, the WGRAD
+// operand quantised by COL_1X16): an item is one 16-row block of one
+// 16-byte column chunk, sixteen 16-byte loads in flight per thread.
+template <typename T>
+__global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParams p) {
+  __shared__ float red[kAmaxThreads / 32];
+  constexpr int kCh = 16 / (int)sizeof(T);  // columns per 16-byte chunk
+  const T* x = static_cast<const T*>(p.x);
+  const int64_t ld = p.ld, cpr = p.cols / kCh, n = (p.rows / 16) * cpr;
+  const uint32_t sign_bits = rht_sign_bits(p.seed);
+  float m = 0.0f;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t jb = q / cpr, cc = q - jb * cpr;
+    const T* base = x + jb * 16 * ld + cc * kCh;
+    uint4 u[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) u[e] = __ldg(reinterpret_cast<const uint4*>(base + e * ld));
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      if (sizeof(T) == 2) {
+        float a[16], b[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t w = wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w;
+          a[e] = __uint_as_float(w << 16);
+          b[e] = __uint_as_float(w & 0xFFFF0000u);
+        }
+        rht16_block(a, sign_bits);
+        rht16_block(b, sign_bits);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m = fmaxf(m, fmaxf(fabsf(a[e]), fabsf(b[e])));
+      } else {
+        float a[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          a[e] = __uint_as_float(wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w);
+        rht16_block(a, sign_bits);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(a[e]));
+      }
+    }
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+}
+
+// max |RHT(x)| with the transform along rows (ROW_1X16 with RHT): an item is
+// one 16-element block of a row.
+template <typename T>
+__global__ void __launch_bounds__(kAmaxThreads) amax_rht_row_kernel(const QParams p) {
+  __shared__ float red[kAmaxThreads / 32];
+  const T* x = static_cast<const T*>(p.x);
+  const int64_t bpr = p.cols / 16, n = p.rows * bpr;
+  const uint32_t sign_bits = rht_sign_bits(p.seed);
+  float m = 0.0f;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = q / bpr, b = q - r * bpr;
+    const T* base = x + r * p.ld + b * 16;
+    float lo[8], hi[8], v[16];
+    load8(base, lo);
+    load8(base + 8, hi);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[e] = lo[e];
+      v[8 + e] = hi[e];
+    }
+    rht16_block(v, sign_bits);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
 
 // ---- host dispatch -------------------------------------------------------------
-template <typename T>
-void launch_amax(const QParams& p, int mode, int grid, cudaStream_t s) {
-  const bool rht = p.flags & NVFP4_RHT;
-  if (mode == NVFP4_COL_1X16 && rht)
-    quant_col_kernel<T, true, false, true><<<grid, kThreads, 0, s>>>(p);
-  else if (mode == NVFP4_ROW_1X16 && rht)
-    quant_row_kernel<T, true, false, true><<<grid, kThreads, 0, s>>>(p);
-  else  // plain max |x| (row, untransformed column, 16x16)
-    quant_row_kernel<T, false, false, true><<<grid, kThreads, 0, s>>>(p);
-}
+// Per-device launch state of one kernel: dynamic shared memory opted in and
+// the number of CTAs that fit on an SM.
+struct LaunchState {
+  std::mutex mu;
+  int per_sm[64] = {};
+};
 
-template <typename T>
-void launch_quant(const QParams& p, int mode, int grid, cudaStream_t s) {
-  const bool rht = p.flags & NVFP4_RHT, sr = p.flags & NVFP4_SR, et = p.flags & NVFP4_EMIT_T;
-  if (mode == NVFP4_ROW_1X16) {
-    if (rht && sr) quant_row_kernel<T, true, true, false><<<grid, kThreads, 0, s>>>(p);
-    else if (rht) quant_row_kernel<T, true, false, false><<<grid, kThreads, 0, s>>>(p);
-    else if (sr) quant_row_kernel<T, false, true, false><<<grid, kThreads, 0, s>>>(p);
-    else quant_row_kernel<T, false, false, false><<<grid, kThreads, 0, s>>>(p);
-  } else if (mode == NVFP4_COL_1X16) {
-    if (rht && sr) quant_col_kernel<T, true, true, false><<<grid, kThreads, 0, s>>>(p);
-    else if (rht) quant_col_kernel<T, true, false, false><<<grid, kThreads, 0, s>>>(p);
-    else if (sr) quant_col_kernel<T, false, true, false><<<grid, kThreads, 0, s>>>(p);
-    else quant_col_kernel<T, false, false, false><<<grid, kThreads, 0, s>>>(p);
-  } else {
-    if (sr && et) quant_16x16_kernel<T, true, true><<<grid, kThreads, 0, s>>>(p);
-    else if (sr) quant_16x16_kernel<T, true, false><<<grid, kThreads, 0, s>>>(p);
-    else if (et) quant_16x16_kernel<T, false, true><<<grid, kThreads, 0, s>>>(p);
-    else quant_16x16_kernel<T, false, false><<<grid, kThreads, 0, s>>>(p);
+template <typename K>
+int resident_per_sm(LaunchState& ls, K kern, int threads, uint32_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(ls.mu);
+  if (ls.per_sm[dev] == 0) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess)
+      return 0;
+    ls.per_sm[dev] = n;
   }
+  return ls.per_sm[dev];
 }
 
-int64_t num_tiles(int mode, int64_t R, int64_t C) {
-  if (mode == NVFP4_ROW_1X16) return ((R + 127) / 128) * ((C + 63) / 64);
-  if (mode == NVFP4_COL_1X16) return ((R + 63) / 64) * ((C + 127) / 128);
-  return ((R + 127) / 128) * ((C + 127) / 128);
+template <auto KERN, class L>
+nvfp4_status launch_q(const CUtensorMap& tm, const QParams& p, int64_t ntiles, int sms,
+                      cudaStream_t s) {
+  static LaunchState ls;
+  const int per_sm = resident_per_sm(ls, KERN, kQThreads, L::kAlloc);
+  if (per_sm <= 0) return NVFP4_ERR_CUDA;
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
+  KERN<<<grid, kQThreads, L::kAlloc, s>>>(tm, p);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+template <auto KERN>
+nvfp4_status launch_amax_kernel(const QParams& p, int grid, cudaStream_t s) {
+  KERN<<<grid, kAmaxThreads, 0, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// Grid of an amax kernel: as many CTAs as are resident at once, at most 4 per
+// SM (the partial-maxima slots a workspace holds) and at most one per 256
+// work items.
+template <auto KERN>
+int amax_grid(int sms, int64_t items) {
+  static LaunchState ls;
+  const int per_sm = std::min(4, std::max(1, resident_per_sm(ls, KERN, kAmaxThreads, 0)));
+  const int64_t want = std::max<int64_t>(1, (items + kAmaxThreads - 1) / kAmaxThreads);
+  return (int)std::min<int64_t>(std::min<int64_t>(want, (int64_t)sms * per_sm), kMaxPartials);
+}
+
+// Amax pre-pass for one quantiser call: returns the CTA count in *grid.
+template <typename T>
+nvfp4_status launch_amax(QParams& p, int mode, int sms, cudaStream_t s) {
+  const bool rht = p.flags & NVFP4_RHT;
+  int grid;
+  if (mode == NVFP4_COL_1X16 && rht) {
+    grid = amax_grid<amax_rht_col_kernel<T>>(sms, (p.rows / 16) * (p.cols * (int64_t)sizeof(T) / 16));
+    p.num_partials = grid;
+    return launch_amax_kernel<amax_rht_col_kernel<T>>(p, grid, s);
+  }
+  if (mode == NVFP4_ROW_1X16 && rht) {
+    grid = amax_grid<amax_rht_row_kernel<T>>(sms, p.rows * (p.cols / 16));
+    p.num_partials = grid;
+    return launch_amax_kernel<amax_rht_row_kernel<T>>(p, grid, s);
+  }
+  grid = amax_grid<amax_plain_kernel<T>>(sms, p.rows * (p.cols / 8) / 4);
+  p.num_partials = grid;
+  return launch_amax_kernel<amax_plain_kernel<T>>(p, grid, s);
+}
+
+// 2-D tensor map over the input [rows, cols] (leading dimension ld): boxes of
+// box_rows x 128 bytes, 128-byte swizzle, zeros outside the tensor.
+template <typename T>
+bool make_input_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                    int box_rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * (int64_t)sizeof(T))};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map,
+             sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+nvfp4_status launch_quant(const QParams& p, int mode, int sms, cudaStream_t s) {
+  const bool rht = p.flags & NVFP4_RHT, sr = p.flags & NVFP4_SR, et = p.flags & NVFP4_EMIT_T;
+  const int64_t R = p.rows, C = p.cols;
+  CUtensorMap tm;
+  if (mode == NVFP4_ROW_1X16) {
+    using G = RowGeo<T>;
+    if (!make_input_map<T>(&tm, p.x, R, C, p.ld, G::kTR)) return NVFP4_ERR_CUDA;
+    const int64_t nt = ((R + G::kTR - 1) / G::kTR) * ((C + G::kTC - 1) / G::kTC);
+    if (rht && sr) return launch_q<quant_row_kernel<T, true, true>, RowL<T>>(tm, p, nt, sms, s);
+    if (rht) return launch_q<quant_row_kernel<T, true, false>, RowL<T>>(tm, p, nt, sms, s);
+    if (sr) return launch_q<quant_row_kernel<T, false, true>, RowL<T>>(tm, p, nt, sms, s);
+    return launch_q<quant_row_kernel<T, false, false>, RowL<T>>(tm, p, nt, sms, s);
+  }
+  if (mode == NVFP4_COL_1X16) {
+    using G = ColGeo<T>;
+    if (!make_input_map<T>(&tm, p.x, R, C, p.ld, G::kTR)) return NVFP4_ERR_CUDA;
+    const int64_t nt = ((R + G::kTR - 1) / G::kTR) * ((C + G::kTC - 1) / G::kTC);
+    if (rht && sr) return launch_q<quant_col_kernel<T, true, true>, ColL<T>>(tm, p, nt, sms, s);
+    if (rht) return launch_q<quant_col_kernel<T, true, false>, ColL<T>>(tm, p, nt, sms, s);
+    if (sr) return launch_q<quant_col_kernel<T, false, true>, ColL<T>>(tm, p, nt, sms, s);
+    return launch_q<quant_col_kernel<T, false, false>, ColL<T>>(tm, p, nt, sms, s);
+  }
+  using G = BlkGeo<T>;
+  if (!make_input_map<T>(&tm, p.x, R, C, p.ld, G::kTR)) return NVFP4_ERR_CUDA;
+  const int64_t nt = ((R + G::kTR - 1) / G::kTR) * ((C + G::kTC - 1) / G::kTC);
+  if (sr && et) return launch_q<quant_16x16_kernel<T, true, true>, BlkL<T>>(tm, p, nt, sms, s);
+  if (sr) return launch_q<quant_16x16_kernel<T, true, false>, BlkL<T>>(tm, p, nt, sms, s);
+  if (et) return launch_q<quant_16x16_kernel<T, false, true>, BlkL<T>>(tm, p, nt, sms, s);
+  return launch_q<quant_16x16_kernel<T, false, false>, BlkL<T>>(tm, p, nt, sms, s);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+nvfp4_status quant_read_error(unsigned int* code) {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero)) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  *code = v;
+  return NVFP4_OK;
+}
 
 // ---- entry point that allocates nothing ---------------------------------------
 // Some callers cannot hand the library a workspace: code that runs while a
@@ -608,6 +1032,8 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
   if (!given && (!workspace || workspace_bytes < kQuantWorkspaceBytes || !aligned16(workspace)))
     return NVFP4_ERR_WORKSPACE;
 
+  if (rows > INT32_MAX || cols > INT32_MAX) return NVFP4_ERR_SHAPE;  // TMA coordinates
+
   DeviceInfo dev;
   nvfp4_status st = current_device(&dev);
   if (st != NVFP4_OK) return st;
@@ -620,6 +1046,7 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
   p.flags = flags;
   p.seed = seed;
   p.offset = offset;
+  p.rk = philox_round_keys(seed);
   p.codes = static_cast<uint8_t*>(out->codes);
   p.scales = static_cast<uint8_t*>(out->scales);
   p.codes_t = static_cast<uint8_t*>(out->codes_t);
@@ -628,24 +1055,20 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
   p.s_dec_out = out->s_dec;
   p.amax_in = out->amax;
   p.partials = static_cast<float*>(workspace);
-
-  const int64_t tiles_amax = num_tiles(
-      (mode == NVFP4_COL_1X16 && (flags & NVFP4_RHT)) ? NVFP4_COL_1X16 : NVFP4_ROW_1X16, rows,
-      cols);
-  const int grid_amax = (int)std::min<int64_t>(
-      std::min<int64_t>(tiles_amax, (int64_t)dev.sm_count * 4), kMaxPartials);
-  p.num_partials = grid_amax;
-  const int64_t tiles = num_tiles(mode, rows, cols);
-  const int grid = (int)std::min<int64_t>(tiles, (int64_t)dev.sm_count * 8);
+  p.num_partials = 0;
+  // 16-byte code stores need 16-byte aligned rows of codes
+  const int64_t code_row_bytes = mode == NVFP4_COL_1X16 ? rows / 2 : cols / 2;
+  p.codes_vec16 = aligned16(out->codes) && code_row_bytes % 16 == 0;
+  p.codes_t_vec8 = (flags & NVFP4_EMIT_T) && (reinterpret_cast<uintptr_t>(out->codes_t) & 7u) == 0;
 
   if (!given) {
-    if (in_dtype == NVFP4_IN_BF16) launch_amax<uint16_t>(p, mode, grid_amax, stream);
-    else launch_amax<float>(p, mode, grid_amax, stream);
-    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    st = in_dtype == NVFP4_IN_BF16 ? launch_amax<uint16_t>(p, mode, dev.sm_count, stream)
+                                   : launch_amax<float>(p, mode, dev.sm_count, stream);
+    if (st != NVFP4_OK) return st;
   }
-  if (in_dtype == NVFP4_IN_BF16) launch_quant<uint16_t>(p, mode, grid, stream);
-  else launch_quant<float>(p, mode, grid, stream);
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  st = in_dtype == NVFP4_IN_BF16 ? launch_quant<uint16_t>(p, mode, dev.sm_count, stream)
+                                 : launch_quant<float>(p, mode, dev.sm_count, stream);
+  if (st != NVFP4_OK) return st;
 
   if (mode == NVFP4_COL_1X16) {
     out->rows = cols;
