@@ -195,7 +195,9 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tenso
 
 /* Output-tile configurations of nvfp4_gemm_ex. */
 enum {
-  NVFP4_TILE_AUTO = 0,          /* 128 x 256 on one SM (128 x 128 when N <= 128)           */
+  NVFP4_TILE_AUTO = 0,          /* 128 x 128 when N <= 128; else the CTA pair when its     *
+                                 * 256 x 256 tiles number at least half the SMs; else      *
+                                 * 128 x 256 on one SM                                     */
   NVFP4_TILE_128X128 = 1,       /* one SM per 128 x 128 tile                               */
   NVFP4_TILE_128X256 = 2,       /* one SM per 128 x 256 tile                               */
   NVFP4_TILE_PAIR_256X256 = 3,  /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */

@@ -34,7 +34,6 @@ namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps
-constexpr int kThreadsPair = 320;
 constexpr int kBM = 128;            // rows of A per tile (one MMA, cta_group::1)
 constexpr int kBKBytes = 128;       // K bytes per stage (256 FP4 elements)
 constexpr int kAtomsPerStage = 4;   // scale atoms per 128 rows per stage (K = 256)
@@ -379,38 +378,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs with tcgen05 cta_group::2.  CTA r loads A rows [128 r, 128 r + 128)
 // and B rows [128 r, 128 r + 128) of the tile, the scale atoms of its A rows
 // and all scale atoms of the tile's B rows; every load completes on the
-// leader's (rank 0) full barrier.  The leader's MMA thread copies one K
-// step's scales ahead of the MMA that reads them and commits to the empty /
-// accumulator barriers of both CTAs.  Each CTA's epilogue drains its 128
-// accumulator rows and releases them on the leader's barrier.  Per SM this
-// moves two thirds of the operand bytes of the single-CTA 128 x 256 tile and
-// reads half the B operand bytes from its own shared memory per MMA.
+// leader's (rank 0) full barrier.  Per SM this moves two thirds of the operand
+// bytes of the single-CTA 128 x 256 tile and reads half the B operand bytes
+// from its own shared memory per MMA.
 //
-// A's scales reach tensor memory with two 128-lane x 256-bit copies per stage
-// instead of four replicating 32x128b.warpx4 copies: the TMA loads an 8 KB
-// image holding each of the stage's four scale atoms four times (row L of an
-// atom's plane is atom row L % 32; the replica dimension of the tensor map
-// has stride 0), so each copy puts two K steps' scales in tensor memory
-// exactly as the warpx4 copies would, at the same 4-aligned columns.  B's
-// scales keep the warpx4 copies.
+// A single thread pays a fixed issue latency per tcgen05 instruction (tens of
+// cycles), so one thread issuing a stage's 12 scale copies and 4 MMAs cannot
+// keep the tensor pipe busy.  The leader therefore splits the issue: the copy
+// warps each wait for the stage's data, issue their share of its 12 scale
+// copies into both CTAs' tensor memory and commit to the stage's scales-ready
+// barrier;
+// the MMA thread waits for that barrier and issues only the MMAs and the
+// commit that frees the stage.  A tensor-memory scale slot is rewritten only
+// after its stage was refilled, i.e. after the MMAs that read it completed.
+// Each CTA's epilogue drains its 128 accumulator rows and releases them on
+// the leader's barrier.
 // =============================================================================
 constexpr int kPairBN = 256;
 
+constexpr int kPairCopyWarps = 2;
+constexpr int kThreadsPairCp = (2 + kPairCopyWarps + 8) * 32;  // producer, MMA, copy, epilogue
+
 template <int STAGES>
 struct PairSmem {
-  static constexpr uint32_t kA = 128 * kBKBytes;          // this CTA's 128 A rows
-  static constexpr uint32_t kB = 128 * kBKBytes;          // this CTA's 128 B rows
-  static constexpr uint32_t kSFA = 8192;  // replicated image of own A rows' scales
-  static constexpr uint32_t kSFB = 2 * kAtomsPerStage * 512;  // the tile's 256 B rows' scales
+  static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
+  static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
+  static constexpr uint32_t kSFA = kAtomsPerStage * 512;       // own A rows' scale atoms
+  static constexpr uint32_t kSFB = 2 * kAtomsPerStage * 512;   // the tile's 256 B rows' scales
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
   static constexpr uint32_t offSFA = offB + STAGES * kB;
   static constexpr uint32_t offSFB = offSFA + STAGES * kSFA;
   static constexpr uint32_t offBar = offSFB + STAGES * kSFB;
-  static constexpr uint32_t kNumBars = 2 * STAGES + 3;
+  static constexpr uint32_t kNumBars = 3 * STAGES + 3 + kPairCopyWarps;  // full, empty, scales-ready, acc x2, drains
   static constexpr uint32_t offMisc = offBar + kNumBars * 8;
-  static constexpr uint32_t kBytes = offMisc + 16;
+  // bf16 output staging for tensor stores: 2 boxes of 32 rows x 64 bytes per
+  // epilogue warp
+  static constexpr uint32_t kStoreBox = 32 * 64;
+  static constexpr uint32_t offStore = (offMisc + 16 + 127) / 128 * 128;
+  static constexpr uint32_t kBytes = offStore + 8 * 2 * kStoreBox;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kSfCol0 = kPairBN;
   static constexpr uint32_t kSfColsPerStage = 16 + 32;  // A (4 K steps x 4), B (4 x 8)
@@ -436,11 +443,12 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
 }
 
 template <int STAGES, int DMODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
-                          const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args) {
+                          const __grid_constant__ CUtensorMap tmSFB,
+                          const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
   using L = PairSmem<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -449,7 +457,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
   const uint32_t bar0 = sbase + L::offBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+  auto sf_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (3 * STAGES);
   const uint32_t acc_empty = acc_full + 8;
   const uint32_t drain_bar = acc_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
@@ -467,10 +476,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sf_bar(s), kPairCopyWarps);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
-    mbar_init(drain_bar, 1);
+    for (int d = 0; d <= kPairCopyWarps; ++d) mbar_init(drain_bar + 8u * d, 1);  // MMA, copy warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -507,10 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
           tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
           tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
                            (b_rb0 + (int)rank) * 128);
-          // A's scale atoms, each replicated 4x (5-D map: byte, atom row,
-          // replica, atom along K, row block)
-          tma_load_5d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, kb * kAtomsPerStage, a_rb);
-          // B's scale atoms as 128-byte rows: 4 atoms = 16 rows per 128 B rows
+          // scale atoms as 128-byte rows: 4 atoms = 16 rows
+          tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
+                           (a_rb * args.kg + kb * kAtomsPerStage) * 4);
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512), &tmSFB,
@@ -522,6 +531,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 200000ull) {
         }
+      }
+    }
+  } else if (warp >= 2 && warp < 2 + kPairCopyWarps) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- scale copies
+      // the stage's copies in the order A atom j (index j), B atom of K step j
+      // and row half hb (index 4 + 2 j + hb); copy warp cw issues the indices
+      // equal to cw modulo the number of copy warps
+      const int cw = warp - 2;
+      uint32_t s = 0, ph = 0;
+      bool ok = true, issued = false;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded_pair(full_bar(s), ph, abort_flag, peer_abort, 0x24u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
+          const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
+          for (int j = 0; j < natoms; ++j) {
+            if (j % kPairCopyWarps == cw)
+              tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+              if ((4 + 2 * j + hb) % kPairCopyWarps == cw)
+                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4 * hb,
+                                          smem_desc_sf(sb + hb * (kAtomsPerStage * 512) + j * 512));
+          }
+          issued = true;
+          tc_commit_pair(sf_bar(s), 1);  // the leader's barrier
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && issued) {  // copies in flight must land before tensor memory is freed
+        tc_commit_pair(drain_bar + 8u * (1 + cw), 1);
+        wait_drain(drain_bar + 8u * (1 + cw), 0);
       }
     }
   } else if (warp == 1) {
@@ -537,7 +586,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded_pair(full_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
+          // the copy warps observed the stage's data, then their copies completed
+          if (!wait_bounded_pair(sf_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
             ok = false;
             break;
           }
@@ -545,23 +595,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
           const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
           const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
-          const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
           const uint32_t a0 = sbase + L::offA + s * L::kA;
           const uint32_t b0 = sbase + L::offB + s * L::kB;
-          auto copy_b_scales = [&](int j) {
-            tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j, smem_desc_sf(sb + j * 512));
-            tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4,
-                                      smem_desc_sf(sb + kAtomsPerStage * 512 + j * 512));
-          };
-          tc_cp_pair_128x256b(sfa_t, smem_desc_sf_image(sa));             // K steps 0, 1
-          if (natoms > 2) tc_cp_pair_128x256b(sfa_t + 8, smem_desc_sf_image(sa + 4096));  // 2, 3
-          copy_b_scales(0);
-          for (int j = 0; j < natoms; ++j) {
-            if (j + 1 < natoms) copy_b_scales(j + 1);  // next step's scales ahead of this MMA
+          for (int j = 0; j < natoms; ++j)
             tc_mma_pair_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
                              idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
-          }
           issued = true;
           tc_commit_pair(empty_bar(s), 3);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -578,9 +616,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     constexpr int kCols = kPairBN / 2, kChunks = kCols / 32;
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int ew = warp - 2 - kPairCopyWarps;  // epilogue warp 0..7
+    const int q = warp & 3, h = ew >> 2;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
     const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
+    uint8_t* stage_out = smem + L::offStore + ew * 2 * L::kStoreBox;
+    if (DMODE == NVFP4_D_BF16 && lane == 0) prefetch_tmap(&tmD);
     uint32_t acc_ph = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
@@ -595,13 +636,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
       acc_ph ^= 1u;
-      const int64_t row = (int64_t)m_blk * 256 + rank * 128 + q * 32 + lane;
+      if (DMODE == NVFP4_D_BF16) {
+        // each 32-column chunk: bf16 rows into a staging box (lane = row; the
+        // 16-byte pieces rotated so a warp's writes hit distinct banks), then
+        // one tensor store; the box is reused two stores later
+        const int32_t row0 = m_blk * 256 + (int)rank * 128 + q * 32;
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int64_t col0 = (int64_t)n_blk * kPairBN + h * kCols + c * 32;
-        if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r[c], alpha);
+        for (int c = 0; c < kChunks; ++c) {
+          uint8_t* box = stage_out + (c & 1) * L::kStoreBox;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__fmul_rn(__uint_as_float(r[c][2 * e]), alpha),
+                                __fmul_rn(__uint_as_float(r[c][2 * e + 1]), alpha));
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc) {
+            const int piece = (pc + (lane >> 1)) & 3;
+            uint4 v;
+            switch (piece) {
+              case 0: v = make_uint4(pk[0], pk[1], pk[2], pk[3]); break;
+              case 1: v = make_uint4(pk[4], pk[5], pk[6], pk[7]); break;
+              case 2: v = make_uint4(pk[8], pk[9], pk[10], pk[11]); break;
+              default: v = make_uint4(pk[12], pk[13], pk[14], pk[15]); break;
+            }
+            *reinterpret_cast<uint4*>(box + lane * 64 + piece * 16) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, smem_u32(box), n_blk * kPairBN + h * kCols + c * 32, row0);
+            bulk_commit_group();
+          }
+        }
+      } else {
+        const int64_t row = (int64_t)m_blk * 256 + rank * 128 + q * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          const int64_t col0 = (int64_t)n_blk * kPairBN + h * kCols + c * 32;
+          if (row < args.M && col0 < args.N) store_row_chunk<DMODE>(args, row, col0, r[c], alpha);
+        }
       }
     }
+    if (DMODE == NVFP4_D_BF16 && lane == 0) bulk_wait_group<0>();  // stores done before exit
   }
 
   tc_fence_before();
@@ -648,25 +726,24 @@ bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 5-D map over a scale tensor that replicates each 512-byte atom four times:
-// dims (16 bytes of an atom row, 32 atom rows, 4 replicas with stride 0,
-// kg atoms along K, row blocks); box = one stage (4 atoms) of one row block.
-bool make_sf_rep_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kg) {
+// 2-D map over a bf16 output [rows, cols] with 32 x 32 boxes (no swizzle);
+// tensor stores skip the part of a box outside the matrix.
+bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const int64_t nrb = (rows + 127) / 128;
-  const cuuint64_t dims[5] = {16, 32, 4, (cuuint64_t)kg, (cuuint64_t)nrb};
-  const cuuint64_t strides[4] = {16, 0, 512, (cuuint64_t)(kg * 512)};
-  const cuuint32_t box[5] = {16, 32, 4, (cuuint32_t)kAtomsPerStage, 1};
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box,
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int STAGES, int DMODE>
 nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
-                         const CUtensorMap& msb, const GemmArgs& a, int sms, cudaStream_t stream) {
+                         const CUtensorMap& msb, const CUtensorMap& md, const GemmArgs& a, int sms,
+                         cudaStream_t stream) {
   using L = PairSmem<STAGES>;
   auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE>;
   static bool configured = false;
@@ -682,7 +759,7 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   if (max_pairs == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(kThreadsPair);
+    cfg.blockDim = dim3(kThreadsPairCp);
     cfg.dynamicSmemBytes = L::kAlloc;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -697,7 +774,7 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   }
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
-  kern<<<grid, kThreadsPair, L::kAlloc, stream>>>(ma, mb, msa, msb, a);
+  kern<<<grid, kThreadsPairCp, L::kAlloc, stream>>>(ma, mb, msa, msb, md, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -750,13 +827,13 @@ nvfp4_status launch_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& m
 
 template <int STAGES>
 nvfp4_status launch_pair_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const CUtensorMap& msa, const CUtensorMap& msb, const GemmArgs& a,
-                              int sms, cudaStream_t s) {
+                              const CUtensorMap& msa, const CUtensorMap& msb,
+                              const CUtensorMap& md, const GemmArgs& a, int sms, cudaStream_t s) {
   switch (d_mode) {
-    case NVFP4_D_BF16: return launch_pair<STAGES, NVFP4_D_BF16>(ma, mb, msa, msb, a, sms, s);
+    case NVFP4_D_BF16: return launch_pair<STAGES, NVFP4_D_BF16>(ma, mb, msa, msb, md, a, sms, s);
     case NVFP4_D_F32_ACCUM:
-      return launch_pair<STAGES, NVFP4_D_F32_ACCUM>(ma, mb, msa, msb, a, sms, s);
-    default: return launch_pair<STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, msa, msb, a, sms, s);
+      return launch_pair<STAGES, NVFP4_D_F32_ACCUM>(ma, mb, msa, msb, md, a, sms, s);
+    default: return launch_pair<STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, msa, msb, md, a, sms, s);
   }
 }
 
@@ -814,7 +891,14 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   nvfp4_status st = current_device(&dev);
   if (st != NVFP4_OK) return st;
 
-  if (tile == NVFP4_TILE_AUTO) tile = N <= 128 ? NVFP4_TILE_128X128 : NVFP4_TILE_128X256;
+  if (tile == NVFP4_TILE_AUTO) {
+    // the CTA pair when its 256 x 256 tiles still give every pair of SMs
+    // work; smaller problems keep more, smaller tiles
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    if (N <= 128) tile = NVFP4_TILE_128X128;
+    else if (pair_tiles >= dev.sm_count / 2) tile = NVFP4_TILE_PAIR_256X256;
+    else tile = NVFP4_TILE_128X256;
+  }
   GemmArgs a;
   a.sfa = static_cast<const uint8_t*>(a_sf);
   a.sfb = static_cast<const uint8_t*>(b_sf);
@@ -830,14 +914,20 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   a.nrb_a = (int)((M + 127) / 128);
   CUtensorMap ma, mb;
   if (tile == NVFP4_TILE_PAIR_256X256) {
-    CUtensorMap msa, msb;
+    CUtensorMap msa, msb, md;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
-        !make_sf_rep_map(&msa, a_sf, M, K / 64) ||
+        !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
         !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
       return NVFP4_ERR_CUDA;
+    // bf16 output map for the tensor-store epilogue (other modes do not use it)
+    if (d_mode == NVFP4_D_BF16) {
+      if (!make_out_map(&md, D, M, N)) return NVFP4_ERR_CUDA;
+    } else {
+      md = ma;
+    }
     a.num_m_blk = (int)((M + 255) / 256);
     a.num_n_blk = (int)((N + 255) / 256);
-    return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, a, dev.sm_count, stream);
+    return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
   }
   const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
   const int mc = tile == NVFP4_TILE_128X256_MC2 ? 2 : 1;
