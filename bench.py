@@ -174,20 +174,24 @@ class Layer:
         X, W, dY = syn.linear_layer(M, K, N)
         self.host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
                      for k, v in (("X", X), ("W", W), ("dY", dY))}
-        self.X = self.host["X"].to(device)
-        self.W = self.host["W"].to(device)
-        self.dY = self.host["dY"].to(device)
+        # two sets of device inputs and outputs: the end-to-end loop copies one
+        # step's data while the previous step computes on the other set
+        self.sets = []
+        for _ in range(2):
+            self.sets.append({
+                "X": self.host["X"].to(device), "W": self.host["W"].to(device),
+                "dY": self.host["dY"].to(device),
+                "Y": torch.empty(M, N, dtype=torch.bfloat16, device=device),
+                "dX": torch.empty(M, K, dtype=torch.bfloat16, device=device),
+                "dW": torch.empty(N, K, dtype=torch.bfloat16, device=device)})
         self.qX = nv.alloc_qtensor(M, K, nv.ROW_1X16, device=device)
         self.qXc = nv.alloc_qtensor(M, K, nv.COL_1X16, device=device)
         self.qW = nv.alloc_qtensor(N, K, nv.BLOCK_16X16, nv.EMIT_T, device=device)
         self.qdY = nv.alloc_qtensor(M, N, nv.ROW_1X16, device=device)
         self.qdYc = nv.alloc_qtensor(M, N, nv.COL_1X16, device=device)
         self.ws = torch.empty(nv.quantize_sizes(M, K, 0)[3], dtype=torch.uint8, device=device)
-        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-        self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=device)
-        self.dW = torch.empty(N, K, dtype=torch.bfloat16, device=device)
-        self.out_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
-                         for k, v in (("Y", self.Y), ("dX", self.dX), ("dW", self.dW))}
+        self.out_host = {k: torch.empty(self.sets[0][k].shape, dtype=torch.bfloat16).pin_memory()
+                         for k in ("Y", "dX", "dW")}
         self.launches_per_step = 5 * 2 + 3
         self.names = ["q_x_row", "q_x_col_rht", "q_w_16x16", "q_dy_row_sr", "q_dy_col_rht_sr",
                       "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
@@ -205,21 +209,21 @@ class Layer:
             b += 2 * elts + elts / 2 * t + (elts / 16 if t == 1 else 2 * elts / 256)
         return b
 
-    def step(self, events=None):
-        nv = self.nv
+    def step(self, events=None, buf=0):
+        nv, d = self.nv, self.sets[buf]
         calls = [
-            lambda: nv.nvfp4_quantize(self.X, nv.ROW_1X16, 0, out=self.qX, workspace=self.ws),
-            lambda: nv.nvfp4_quantize(self.X, nv.COL_1X16, nv.RHT, seed=0, out=self.qXc,
+            lambda: nv.nvfp4_quantize(d["X"], nv.ROW_1X16, 0, out=self.qX, workspace=self.ws),
+            lambda: nv.nvfp4_quantize(d["X"], nv.COL_1X16, nv.RHT, seed=0, out=self.qXc,
                                       workspace=self.ws),
-            lambda: nv.nvfp4_quantize(self.W, nv.BLOCK_16X16, nv.EMIT_T, out=self.qW,
+            lambda: nv.nvfp4_quantize(d["W"], nv.BLOCK_16X16, nv.EMIT_T, out=self.qW,
                                       workspace=self.ws),
-            lambda: nv.nvfp4_quantize(self.dY, nv.ROW_1X16, nv.SR, seed=0, offset=0,
+            lambda: nv.nvfp4_quantize(d["dY"], nv.ROW_1X16, nv.SR, seed=0, offset=0,
                                       out=self.qdY, workspace=self.ws),
-            lambda: nv.nvfp4_quantize(self.dY, nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1,
+            lambda: nv.nvfp4_quantize(d["dY"], nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1,
                                       out=self.qdYc, workspace=self.ws),
-            lambda: nv.nvfp4_gemm(self.qX, self.qW, out=self.Y),
-            lambda: nv.nvfp4_gemm(self.qdY, self.qW, b_view=1, out=self.dX),
-            lambda: nv.nvfp4_gemm(self.qdYc, self.qXc, out=self.dW),
+            lambda: nv.nvfp4_gemm(self.qX, self.qW, out=d["Y"]),
+            lambda: nv.nvfp4_gemm(self.qdY, self.qW, b_view=1, out=d["dX"]),
+            lambda: nv.nvfp4_gemm(self.qdYc, self.qXc, out=d["dW"]),
         ]
         for i, c in enumerate(calls):
             if events is not None:
@@ -288,18 +292,39 @@ def run_ours(args):
     # ---- end to end through host buffers (H2D inputs, D2H outputs) ----------
     h2d = sum(t.numel() * t.element_size() for t in layer.host.values())
     d2h = sum(t.numel() * t.element_size() for t in layer.out_host.values())
+    # Pipelined like a training loop: step i's inputs go host -> device on one
+    # copy stream and step i-1's outputs device -> host on another while the
+    # compute stream runs; two sets of device buffers, ordered by events.
+    # Every step's copies lie inside the timed region.
+    cur = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set b landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # compute on set b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # outputs of set b copied out
+    for b in range(2):
+        ev_used[b].record(cur)
+        ev_out[b].record(cur)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        layer.X.copy_(layer.host["X"], non_blocking=True)
-        layer.W.copy_(layer.host["W"], non_blocking=True)
-        layer.dY.copy_(layer.host["dY"], non_blocking=True)
-        layer.step()
-        layer.out_host["Y"].copy_(layer.Y, non_blocking=True)
-        layer.out_host["dX"].copy_(layer.dX, non_blocking=True)
-        layer.out_host["dW"].copy_(layer.dW, non_blocking=True)
-        torch.cuda.synchronize()
+    for i in range(args.e2e_steps):
+        b = i % 2
+        d = layer.sets[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[b])  # the step that last read set b is done
+            for k in ("X", "W", "dY"):
+                d[k].copy_(layer.host[k], non_blocking=True)
+            ev_in[b].record(s_in)
+        cur.wait_event(ev_in[b])
+        cur.wait_event(ev_out[b])        # set b's previous outputs were copied out
+        layer.step(buf=b)
+        ev_used[b].record(cur)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[b])
+            for k in ("Y", "dX", "dW"):
+                layer.out_host[k].copy_(d[k], non_blocking=True)
+            ev_out[b].record(s_out)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, device)
     e2e_value = world * layer.flops() / e2e_s / 1e12
 
