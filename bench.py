@@ -34,6 +34,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roofline"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
+# DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM at
+# M=8192, N=14336, K=4096, from one ncu capture of that launch
+# (dram__bytes_read.sum 53.2 MB + dram__bytes_write.sum 188.1 MB); None once
+# the kernel changes after the capture.
+FPROP_TRAFFIC_BYTES = 53.193472e6 + 188.105728e6
+FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
         "dY ~ N(0,1e-3), bf16")
@@ -332,9 +338,13 @@ def run_ours(args):
         return
     peaks, peak_src = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
-    gemm_ms = statistics.mean(kern_ms[k] for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad"))
+    # roofline of the dominant kernel: the FPROP GEMM launch (the three GEMMs
+    # take the same time within a few percent; see kernels_ms)
+    gemm_ms = kern_ms["gemm_fprop"]
     gemm_flops = 2.0 * args.m * args.n * args.k
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    traffic = (FPROP_TRAFFIC_BYTES if FPROP_TRAFFIC_BYTES is not None
+               and (args.m, args.k, args.n) == FPROP_TRAFFIC_SHAPE else None)
     q_ms = sum(kern_ms[k] for k in layer.names if k.startswith("q_"))
     q_gbs = layer.quant_bytes() / (q_ms * 1e-3) / 1e9
     line = {
@@ -347,11 +357,15 @@ def run_ours(args):
                    "M": args.m, "K": args.k, "N": args.n,
                    "l2": "flushed before every timed step, untimed: 256 MiB device write, then 256 MiB device read (L2 starts cold and clean)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_nvf4 (mean of FPROP/DGRAD/WGRAD)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "gemm_nvf4_pair_kernel, FPROP launch (one 2MNK GEMM per launch)",
                      "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
                      "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)",
-                     "traffic": None},
+                     "traffic": traffic, "traffic_unit": "bytes per launch",
+                     "algorithmic_bytes": round(args.m * args.k / 2 + args.n * args.k / 2
+                                                + (args.m + args.n) * args.k / 16
+                                                + 2 * args.m * args.n)},
         "quantize": {"gbs": round(q_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                      "frac": round(q_gbs / peaks["hbm_gbs"], 4),
                      "ms_per_step": round(q_ms, 4),
