@@ -198,9 +198,11 @@ class Layer:
         self.ws = torch.empty(nv.quantize_sizes(M, K, 0)[3], dtype=torch.uint8, device=device)
         self.out_host = {k: torch.empty(self.sets[0][k].shape, dtype=torch.bfloat16).pin_memory()
                          for k in ("Y", "dX", "dW")}
-        self.launches_per_step = 5 * 2 + 3
-        self.names = ["q_x_row", "q_x_col_rht", "q_w_16x16", "q_dy_row_sr", "q_dy_col_rht_sr",
-                      "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
+        # launches per step: one-read amax of X and of dY (2 each), 4 given-amax
+        # quantise passes, W's quantiser (amax pass + quantise pass), 3 GEMMs
+        self.launches_per_step = 2 * 2 + 4 + 2 + 3
+        self.names = ["q_x_amax", "q_x_row", "q_x_col_rht", "q_w_16x16", "q_dy_amax",
+                      "q_dy_row_sr", "q_dy_col_rht_sr", "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
 
     def flops(self):
         return 3 * 2.0 * self.M * self.N * self.K
@@ -217,16 +219,19 @@ class Layer:
 
     def step(self, events=None, buf=0):
         nv, d = self.nv, self.sets[buf]
+        G = nv.AMAX_GIVEN
         calls = [
-            lambda: nv.nvfp4_quantize(d["X"], nv.ROW_1X16, 0, out=self.qX, workspace=self.ws),
-            lambda: nv.nvfp4_quantize(d["X"], nv.COL_1X16, nv.RHT, seed=0, out=self.qXc,
-                                      workspace=self.ws),
+            lambda: nv.nvfp4_amax(d["X"], self.qX.amax, self.qXc.amax, seed=0, workspace=self.ws),
+            lambda: nv.nvfp4_quantize(d["X"], nv.ROW_1X16, G, out=self.qX),
+            lambda: nv.nvfp4_quantize(d["X"], nv.COL_1X16, nv.RHT | G, seed=0, out=self.qXc),
             lambda: nv.nvfp4_quantize(d["W"], nv.BLOCK_16X16, nv.EMIT_T, out=self.qW,
                                       workspace=self.ws),
-            lambda: nv.nvfp4_quantize(d["dY"], nv.ROW_1X16, nv.SR, seed=0, offset=0,
-                                      out=self.qdY, workspace=self.ws),
-            lambda: nv.nvfp4_quantize(d["dY"], nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1,
-                                      out=self.qdYc, workspace=self.ws),
+            lambda: nv.nvfp4_amax(d["dY"], self.qdY.amax, self.qdYc.amax, seed=0,
+                                  workspace=self.ws),
+            lambda: nv.nvfp4_quantize(d["dY"], nv.ROW_1X16, nv.SR | G, seed=0, offset=0,
+                                      out=self.qdY),
+            lambda: nv.nvfp4_quantize(d["dY"], nv.COL_1X16, nv.RHT | nv.SR | G, seed=0, offset=1,
+                                      out=self.qdYc),
             lambda: nv.nvfp4_gemm(self.qX, self.qW, out=d["Y"]),
             lambda: nv.nvfp4_gemm(self.qdY, self.qW, b_view=1, out=d["dX"]),
             lambda: nv.nvfp4_gemm(self.qdYc, self.qXc, out=d["dW"]),

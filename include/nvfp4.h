@@ -146,6 +146,28 @@ nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64
                             uint64_t offset, nvfp4_tensor* out, void* workspace,
                             size_t workspace_bytes, nvfp4_stream stream);
 
+/* The per-tensor amax of nvfp4_quantize ("NVFP4 pretraining recipe", bullet
+ * 4: amax_T over the operand as quantised) for the two quantisations a
+ * training step makes of X and of dY -- the row-wise operand (ROW_1X16, no
+ * transform) and the column-wise WGRAD operand (COL_1X16 with NVFP4_RHT) --
+ * from one read of x [rows, cols] (leading dim ld, bf16 or fp32):
+ *   amax_plain = max |x|                            (if amax_plain != NULL),
+ *   amax_rht   = max |(1/4) H16 diag(s) v| over every 16-row block v of every
+ *                column, signs s from `seed` as in nvfp4_quantize
+ *                                                   (if amax_rht != NULL).
+ * Both are device floats; each equals, bit for bit, the amax the matching
+ * nvfp4_quantize call computes itself, so passing it with NVFP4_AMAX_GIVEN
+ * (out->amax pointing at it) gives identical codes and scales.  At least one
+ * output must be non-NULL; amax_rht needs rows % 16 == 0.  x: 16-byte
+ * aligned, ld * element size a multiple of 16 bytes, cols % 8 == 0.  The
+ * workspace is as for nvfp4_quantize (partial maxima; contents on return
+ * unspecified).  Two kernel launches on `stream`; nothing is allocated.
+ * Returns NVFP4_ERR_INVALID_ARG, _SHAPE, _ALIGN, _WORKSPACE, _ARCH, _CUDA as
+ * nvfp4_quantize does. */
+nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                        uint64_t seed, float* amax_plain, float* amax_rht, void* workspace,
+                        size_t workspace_bytes, nvfp4_stream stream);
+
 /* nvfp4_quantize without a workspace argument; the paper has no counterpart
  * to this entry point.  It is for callers that cannot provide device scratch
  * memory -- code running during CUDA graph capture (where cudaMalloc is not

@@ -65,6 +65,7 @@ def _load():
                            C.c_int),
         "nvfp4_quantize_noalloc": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp],
                                    C.c_int),
+        "nvfp4_amax": ([vp, i32, i64, i64, i64, u64, vp, vp, vp, sz, vp], C.c_int),
         "nvfp4_gemm": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, vp, sz, vp],
                        C.c_int),
         "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
@@ -184,6 +185,28 @@ def nvfp4_quantize(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0, of
                               0 if workspace is None else workspace.numel(), _stream(stream)),
            "nvfp4_quantize")
     return out
+
+
+def nvfp4_amax(x: torch.Tensor, amax_plain: torch.Tensor | None = None,
+               amax_rht: torch.Tensor | None = None, seed: int = 0,
+               workspace: torch.Tensor | None = None, stream=None):
+    """max |x| and/or max |RHT(x)| along columns from one read (see nvfp4_amax
+    in nvfp4.h); the outputs are 1-element float32 CUDA tensors, e.g. the
+    `amax` of the QTensors then quantised with NVFP4_AMAX_GIVEN."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    dt = {torch.bfloat16: IN_BF16, torch.float32: IN_FP32}.get(x.dtype)
+    if dt is None:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    for t in (amax_plain, amax_rht):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != 1 or not t.is_cuda):
+            raise ValueError("amax outputs must be 1-element float32 CUDA tensors")
+    rows, cols = x.shape
+    if workspace is None:
+        workspace = _workspace(quantize_sizes(rows, cols, ROW_1X16)[3], x.device)
+    _check(lib.nvfp4_amax(x.data_ptr(), dt, rows, cols, x.stride(0), seed, _ptr(amax_plain),
+                          _ptr(amax_rht), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "nvfp4_amax")
 
 
 def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0,

@@ -96,6 +96,13 @@ nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64
                        workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                        uint64_t seed, float* amax_plain, float* amax_rht, void* workspace,
+                        size_t workspace_bytes, nvfp4_stream stream) {
+  return amax_impl(x, in_dtype, rows, cols, ld, seed, amax_plain, amax_rht, workspace,
+                   workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                         int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
                         int64_t N, int64_t K, void* workspace, size_t workspace_bytes,

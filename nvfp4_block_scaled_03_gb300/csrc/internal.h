@@ -51,6 +51,10 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder();
 
+nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                       uint64_t seed, float* amax_plain, float* amax_rht, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
 // Reads and clears the quantisers' device error word (after a sync).
 nvfp4_status quant_read_error(unsigned int* code);
 

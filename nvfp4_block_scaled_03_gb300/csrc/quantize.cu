@@ -723,10 +723,13 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_plain_kernel(const QParams 
 
 // max |RHT(x)| with the transform along columns (16-row blocks, the WGRAD
 // operand quantised by COL_1X16): an item is one 16-row block of one
-// 16-byte column chunk, sixteen 16-byte loads in flight per thread.
-template <typename T>
+// 16-byte column chunk, sixteen 16-byte loads in flight per thread.  With
+// PLAIN it also takes max |x| of the same values (every element, as rows are
+// whole 16-row blocks), written to the upper half of the partials.
+template <typename T, bool PLAIN>
 __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParams p) {
   __shared__ float red[kAmaxThreads / 32];
+  float mp = 0.0f;
   constexpr int kCh = 16 / (int)sizeof(T);  // columns per 16-byte chunk
   const T* x = static_cast<const T*>(p.x);
   const int64_t ld = p.ld, cpr = p.cols / kCh, n = (p.rows / 16) * cpr;
@@ -748,6 +751,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
           const uint32_t w = wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w;
           a[e] = __uint_as_float(w << 16);
           b[e] = __uint_as_float(w & 0xFFFF0000u);
+          if (PLAIN) mp = fmaxf(mp, fmaxf(fabsf(a[e]), fabsf(b[e])));
         }
         rht16_block(a, sign_bits);
         rht16_block(b, sign_bits);
@@ -756,8 +760,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
       } else {
         float a[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
+        for (int e = 0; e < 16; ++e) {
           a[e] = __uint_as_float(wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w);
+          if (PLAIN) mp = fmaxf(mp, fabsf(a[e]));
+        }
         rht16_block(a, sign_bits);
 #pragma unroll
         for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(a[e]));
@@ -766,6 +772,29 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+  if (PLAIN) {
+    mp = block_max(mp, red);
+    if (threadIdx.x == 0) p.partials[kMaxPartials / 2 + blockIdx.x] = mp;
+  }
+}
+
+// Final reduction of an nvfp4_amax call: partials [0, n) to *out0 and, when
+// out1 is set, partials [kMaxPartials / 2, + n) to *out1.
+__global__ void __launch_bounds__(kAmaxThreads) amax_finalize_kernel(const float* partials,
+                                                                     int n, float* out0,
+                                                                     float* out1) {
+  __shared__ float red[kAmaxThreads / 32];
+  float m0 = 0.0f, m1 = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    m0 = fmaxf(m0, partials[i]);
+    if (out1) m1 = fmaxf(m1, partials[kMaxPartials / 2 + i]);
+  }
+  m0 = block_max(m0, red);
+  if (threadIdx.x == 0) *out0 = m0;
+  if (out1) {
+    m1 = block_max(m1, red);
+    if (threadIdx.x == 0) *out1 = m1;
+  }
 }
 
 // max |RHT(x)| with the transform along rows (ROW_1X16 with RHT): an item is
@@ -857,9 +886,10 @@ nvfp4_status launch_amax(QParams& p, int mode, int sms, cudaStream_t s) {
   const bool rht = p.flags & NVFP4_RHT;
   int grid;
   if (mode == NVFP4_COL_1X16 && rht) {
-    grid = amax_grid<amax_rht_col_kernel<T>>(sms, (p.rows / 16) * (p.cols * (int64_t)sizeof(T) / 16));
+    grid = amax_grid<amax_rht_col_kernel<T, false>>(
+        sms, (p.rows / 16) * (p.cols * (int64_t)sizeof(T) / 16));
     p.num_partials = grid;
-    return launch_amax_kernel<amax_rht_col_kernel<T>>(p, grid, s);
+    return launch_amax_kernel<amax_rht_col_kernel<T, false>>(p, grid, s);
   }
   if (mode == NVFP4_ROW_1X16 && rht) {
     grid = amax_grid<amax_rht_row_kernel<T>>(sms, p.rows * (p.cols / 16));
@@ -924,6 +954,60 @@ nvfp4_status launch_quant(const QParams& p, int mode, int sms, cudaStream_t s) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// One read of x for the amax of its row-wise and column-wise (RHT) quantisations.
+nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                       uint64_t seed, float* amax_plain, float* amax_rht, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || (!amax_plain && !amax_rht)) return NVFP4_ERR_INVALID_ARG;
+  if (in_dtype != NVFP4_IN_BF16 && in_dtype != NVFP4_IN_FP32) return NVFP4_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || cols % 8) return NVFP4_ERR_SHAPE;
+  if (amax_rht && rows % 16) return NVFP4_ERR_SHAPE;
+  const int64_t esz = in_dtype == NVFP4_IN_BF16 ? 2 : 4;
+  if (!aligned16(x) || (ld * esz) % 16) return NVFP4_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(amax_plain) & 3u) || (reinterpret_cast<uintptr_t>(amax_rht) & 3u))
+    return NVFP4_ERR_ALIGN;
+  if (!workspace || workspace_bytes < kQuantWorkspaceBytes || !aligned16(workspace))
+    return NVFP4_ERR_WORKSPACE;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+
+  QParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.ld = ld;
+  p.seed = seed;
+  p.partials = static_cast<float*>(workspace);
+  const bool bf = in_dtype == NVFP4_IN_BF16;
+  int grid = 0;
+  if (!amax_rht) {  // max |x| alone
+    grid = bf ? amax_grid<amax_plain_kernel<uint16_t>>(dev.sm_count, rows * (cols / 8) / 4)
+              : amax_grid<amax_plain_kernel<float>>(dev.sm_count, rows * (cols / 8) / 4);
+    st = bf ? launch_amax_kernel<amax_plain_kernel<uint16_t>>(p, grid, stream)
+            : launch_amax_kernel<amax_plain_kernel<float>>(p, grid, stream);
+  } else {  // the RHT amax, with max |x| from the same loads when asked for
+    const int64_t items = (rows / 16) * (cols * esz / 16);
+    if (amax_plain) {
+      grid = bf ? amax_grid<amax_rht_col_kernel<uint16_t, true>>(dev.sm_count, items)
+                : amax_grid<amax_rht_col_kernel<float, true>>(dev.sm_count, items);
+      grid = std::min(grid, kMaxPartials / 2);
+      st = bf ? launch_amax_kernel<amax_rht_col_kernel<uint16_t, true>>(p, grid, stream)
+              : launch_amax_kernel<amax_rht_col_kernel<float, true>>(p, grid, stream);
+    } else {
+      grid = bf ? amax_grid<amax_rht_col_kernel<uint16_t, false>>(dev.sm_count, items)
+                : amax_grid<amax_rht_col_kernel<float, false>>(dev.sm_count, items);
+      st = bf ? launch_amax_kernel<amax_rht_col_kernel<uint16_t, false>>(p, grid, stream)
+              : launch_amax_kernel<amax_rht_col_kernel<float, false>>(p, grid, stream);
+    }
+  }
+  if (st != NVFP4_OK) return st;
+  float* out0 = amax_rht ? amax_rht : amax_plain;
+  float* out1 = amax_rht ? amax_plain : nullptr;
+  amax_finalize_kernel<<<1, kAmaxThreads, 0, stream>>>(p.partials, grid, out0, out1);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
 
 nvfp4_status quant_read_error(unsigned int* code) {
   unsigned int v = 0, zero = 0;

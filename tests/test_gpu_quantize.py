@@ -139,3 +139,52 @@ def test_quantize_32k_tokens_sampled(nv, orc, mode_name, spec):
         assert np.array_equal(scales[rb * atom_bytes:(rb + 1) * atom_bytes], o["scales_sw"])
         if not flags & orc.SR:
             assert np.array_equal(codes[sl], o["codes"])
+
+
+@pytest.mark.parametrize("shape,kind,dtype", [((336, 400), "dy", "bf16"), ((128, 256), "x", "fp32"),
+                                              ((8192, 14336), "dy", "bf16")])
+def test_amax_one_read_matches_oracle_and_quantise(nv, orc, shape, kind, dtype):
+    """nvfp4_amax: max |x| and the column-RHT amax from one read equal the
+    oracle's; quantising with them given reproduces the self-computed codes."""
+    import torch
+    x = _input(shape, kind, dtype)
+    xt = H.dev_bf16(x) if x.dtype == np.uint16 else H.dev_f32(x)
+    seed = 5
+    a_plain = torch.zeros(1, dtype=torch.float32, device="cuda")
+    a_rht = torch.zeros(1, dtype=torch.float32, device="cuda")
+    nv.nvfp4_amax(xt, a_plain, a_rht, seed=seed)
+    assert float(a_plain.cpu()[0]) == orc.amax(x, orc.ROW_1X16, 0, seed=seed)
+    assert float(a_rht.cpu()[0]) == orc.amax(x, orc.COL_1X16, orc.RHT, seed=seed)
+    # each output alone takes another kernel path; same values
+    b_plain = torch.zeros(1, dtype=torch.float32, device="cuda")
+    b_rht = torch.zeros(1, dtype=torch.float32, device="cuda")
+    nv.nvfp4_amax(xt, amax_plain=b_plain, seed=seed)
+    nv.nvfp4_amax(xt, amax_rht=b_rht, seed=seed)
+    assert float(b_plain.cpu()[0]) == float(a_plain.cpu()[0])
+    assert float(b_rht.cpu()[0]) == float(a_rht.cpu()[0])
+    for mode, flags, a in ((nv.ROW_1X16, nv.SR, a_plain), (nv.COL_1X16, nv.RHT | nv.SR, a_rht)):
+        ref = nv.nvfp4_quantize(xt, mode, flags, seed=seed, offset=2)
+        q = nv.alloc_qtensor(shape[0], shape[1], mode, flags)
+        q.amax.copy_(a)
+        nv.nvfp4_quantize(xt, mode, flags | nv.AMAX_GIVEN, seed=seed, offset=2, out=q)
+        for name in ("codes", "scales", "amax", "s_dec"):
+            assert torch.equal(getattr(q, name), getattr(ref, name)), name
+    if shape[0] * shape[1] <= 1 << 20:  # and against the oracle directly
+        q = nv.alloc_qtensor(shape[0], shape[1], nv.COL_1X16, nv.RHT)
+        q.amax.copy_(a_rht)
+        nv.nvfp4_quantize(xt, nv.COL_1X16, nv.RHT | nv.AMAX_GIVEN, seed=seed, out=q)
+        H.assert_quant_equal(q, orc.quantize(x, orc.COL_1X16, orc.RHT, seed=seed), "rht given")
+
+
+def test_amax_rejects_bad_arguments(nv):
+    import torch
+    x = torch.zeros(40, 32, dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_amax(x, amax_rht=a)                 # 40 % 16: no whole RHT blocks
+    assert e.value.status == nv.ERR_SHAPE
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_amax(x)                             # no output asked for
+    assert e.value.status == nv.ERR_INVALID_ARG
+    nv.nvfp4_amax(x, amax_plain=a)                   # the plain amax has no row constraint
+    assert float(a.cpu()[0]) == 0.0
