@@ -621,13 +621,17 @@ __global__ void __launch_bounds__(kQThreads, 2)
       ok_s[rl16 * kKWords + 2 * b + h] = packed;
       scw |= sc << (8 * b);
       if (EMIT_T) {
+        // transposed byte of column e = code(even row, e) | code(odd row, e) << 4:
+        // t holds columns 0, 2, 4, 6 and u columns 1, 3, 5, 7 of the lane
+        // pair's 8 columns; the even lane stores columns 0-3, the odd 4-7
         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, packed, 1);  // row rl ^ 1
-        if ((lane & 1) == 0) {
+        const uint32_t lo = (lane & 1) ? other : packed, hi = (lane & 1) ? packed : other;
+        const uint32_t t = (lo & 0x0F0F0F0Fu) | ((hi & 0x0F0F0F0Fu) << 4);
+        const uint32_t u = ((lo >> 4) & 0x0F0F0F0Fu) | (hi & 0xF0F0F0F0u);
+        const uint32_t w = (lane & 1) ? __byte_perm(t, u, 0x7362) : __byte_perm(t, u, 0x5140);
+        const int cb = 16 * b + 8 * h + 4 * (lane & 1);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            ot_s[(16 * b + 8 * h + e) * 8 + (rl16 >> 1)] =
-                (uint8_t)(((packed >> (4 * e)) & 0xFu) | (((other >> (4 * e)) & 0xFu) << 4));
-        }
+        for (int k = 0; k < 4; ++k) ot_s[(cb + k) * 8 + (rl16 >> 1)] = (uint8_t)(w >> (8 * k));
         // transposed scale of output row c0 + 16 b + lane, scale column g
         if (lane < 16 && g < 4 * apr_t) {
           const int64_t orow = c0 + 16 * b + lane;
@@ -690,32 +694,33 @@ __global__ void __launch_bounds__(kQThreads, 2)
 // Amax pre-pass: per-CTA partial maxima of |x| (or of |RHT(x)| along the
 // dimension the quantiser transforms), written to the workspace.
 // =============================================================================
-// max |x|: 8-element chunks, four 16-byte loads in flight per thread.
+// max |x|: 8-element chunks, eight 16-byte loads in flight per thread (the
+// pass is bound by how many bytes each SM keeps in flight).
 template <typename T>
 __global__ void __launch_bounds__(kAmaxThreads) amax_plain_kernel(const QParams p) {
+  constexpr int kU = 8;
   __shared__ float red[kAmaxThreads / 32];
   const T* x = static_cast<const T*>(p.x);
   const int64_t C = p.cols, ld = p.ld, cpr = C / 8, n = p.rows * cpr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   float m = 0.0f;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += 4 * stride) {
-    float v[4][8];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += kU * stride) {
+    // all loads issued before any value is used: indices past the end are
+    // clamped to the last chunk (a valid address) and their values dropped
+    float v[kU][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t q = i + u * stride;
-      if (q < n) {
-        const int64_t r = ld == C ? 0 : q / cpr;
-        const int64_t off = ld == C ? q * 8 : r * ld + (q - r * cpr) * 8;
-        load8(x + off, v[u]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
-      }
+    for (int u = 0; u < kU; ++u) {
+      const int64_t q = min(i + u * stride, n - 1);
+      const int64_t r = ld == C ? 0 : q / cpr;
+      const int64_t off = ld == C ? q * 8 : r * ld + (q - r * cpr) * 8;
+      load8(x + off, v[u]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kU; ++u)
+      if (i + u * stride < n) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+      }
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
