@@ -80,6 +80,8 @@ def lib():
                 "orc_swizzle_offset": ([i64, i64, i64], i64),
                 "orc_quantize": ([vp, C.c_int, i64, i64, i64, C.c_int, u32, u64, u64, f32,
                                   C.POINTER(_QOut)], C.c_int),
+                "orc_quantize_window": ([vp, C.c_int, i64, i64, i64, C.c_int, u32, u64, u64, f32,
+                                         u64, C.POINTER(_QOut)], C.c_int),
                 "orc_amax": ([vp, C.c_int, i64, i64, i64, C.c_int, u32, u64], f32),
                 "orc_dequant": ([vp, vp, f32, i64, i64, vp], None),
                 "orc_gemm_fp64": ([vp, vp, f32, vp, vp, f32, i64, i64, i64, vp], None),
@@ -179,8 +181,12 @@ def swizzle_offset(r: int, c: int, ocols: int) -> int:
 
 
 def quantize(x: np.ndarray, mode: int, flags: int = 0, seed: int = 0, offset: int = 0,
-             amax_given: float | None = None) -> dict:
+             amax_given: float | None = None, sr_index_base: int = 0) -> dict:
     """Quantise a 2-D bf16 (uint16 bit patterns) or float32 array.
+
+    ``sr_index_base`` evaluates a window of output rows of a larger operand:
+    each element's stochastic-rounding index is its index in the window plus
+    the base (the window's first output row times the output columns).
 
     Returns a dict with ``codes`` [orows, ocols/2] uint8, ``scales`` [orows,
     ocols/16] uint8 (row-major E4M3), ``scales_sw`` (MMA layout, padded),
@@ -215,8 +221,8 @@ def quantize(x: np.ndarray, mode: int, flags: int = 0, seed: int = 0, offset: in
                                                 res["scales_t_sw"].ctypes.data)
     if amax_given is not None:
         flags |= AMAX_GIVEN
-    rc = lib().orc_quantize(_p(x), dt, rows, cols, cols, mode, flags, seed, offset,
-                            float(amax_given or 0.0), C.byref(q))
+    rc = lib().orc_quantize_window(_p(x), dt, rows, cols, cols, mode, flags, seed, offset,
+                                   float(amax_given or 0.0), int(sr_index_base), C.byref(q))
     if rc != 0:
         raise ValueError(f"oracle quantize rejected its arguments (rc={rc})")
     res["scales_sw"] = res["scales_sw"][:swizzled_bytes(orows, ocols)]

@@ -343,6 +343,13 @@ static void swizzle_scales(const uint8_t* rm, int64_t orows, int64_t ocols, uint
 int orc_quantize(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
                  int mode, uint32_t flags, uint64_t seed, uint64_t offset,
                  float amax_given, orc_qout* out) {
+  return orc_quantize_window(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, amax_given,
+                             0, out);
+}
+
+int orc_quantize_window(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                        int mode, uint32_t flags, uint64_t seed, uint64_t offset,
+                        float amax_given, uint64_t sr_index_base, orc_qout* out) {
   if (check_args(in_dtype, rows, cols, ld, mode, flags)) return 1;
   if (!out || !out->codes || !out->scales) return 1;
   if ((flags & ORC_EMIT_T) && (!out->codes_t || !out->scales_t)) return 1;
@@ -394,7 +401,7 @@ int orc_quantize(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_
       float enc = encode_factor(out->scales[r * nsc + c / 16], s_enc);
       float y = v[r * ocols + c] * enc;
       uint8_t code;
-      if (flags & ORC_SR) code = orc_e2m1_sr(y, orc_sr_word(seed, offset, (uint64_t)(r * ocols + c)));
+      if (flags & ORC_SR) code = orc_e2m1_sr(y, orc_sr_word(seed, offset, sr_index_base + (uint64_t)(r * ocols + c)));
       else                code = orc_e2m1_rne(y);
       put_code(out->codes + r * (ocols / 2), c, code);
       if (flags & ORC_EMIT_T) put_code(out->codes_t + c * (orows / 2), r, code);

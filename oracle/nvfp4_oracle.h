@@ -74,6 +74,15 @@ int orc_quantize(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_
                  int mode, uint32_t flags, uint64_t seed, uint64_t offset,
                  float amax_given, orc_qout* out);
 
+/* orc_quantize of a window of output rows of a larger operand: x holds the
+ * window alone, and every element's stochastic-rounding index is its index in
+ * the whole operand's output, i.e. its index in the window plus sr_index_base
+ * (= first output row of the window * output columns).  Same arithmetic;
+ * orc_quantize is this with sr_index_base = 0. */
+int orc_quantize_window(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                        int mode, uint32_t flags, uint64_t seed, uint64_t offset,
+                        float amax_given, uint64_t sr_index_base, orc_qout* out);
+
 /* Amax of the (optionally RHT'd) operand, as the quantiser computes it. */
 float orc_amax(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
                int mode, uint32_t flags, uint64_t seed);

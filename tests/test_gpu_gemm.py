@@ -132,3 +132,42 @@ def test_gemm_llama8b_full_sampled(nv, orc):
         got = H.host_f64(D[m, n])
         H.assert_gemm_close(got, ref, name)
         del A, B, D
+
+
+def test_gemm_405b_up_projection_full_sampled(nv, orc):
+    """The Llama-3.1-405B MLP up projection at full size (X [8192, 16384],
+    W [53248, 16384], dY [8192, 53248]): FPROP (K = 16384), DGRAD through W's
+    transposed view (K = 53248) and WGRAD (K = 8192), each on oracle-quantised
+    operands, checked on 4096 random outputs plus the first and last 128x128
+    tiles."""
+    import gc
+    M, K, N = 8192, 16384, 53248
+    X = syn.activations((M, K), seed=1)
+    W = syn.weights((N, K), seed=2)
+    qW = orc.quantize(W, orc.BLOCK_16X16, orc.EMIT_T)
+    del W
+    gc.collect()
+    qX = orc.quantize(X, orc.ROW_1X16)
+    _check_sampled(nv, orc, "FPROP 405B", qX, qW)
+    del qX
+    gc.collect()
+    dY = syn.gradients((M, N), seed=3)
+    qdY = orc.quantize(dY, orc.ROW_1X16, orc.SR, seed=0, offset=0)
+    _check_sampled(nv, orc, "DGRAD 405B", qdY, orc.transposed_view(qW))
+    del qdY, qW
+    gc.collect()
+    qdYc = orc.quantize(dY, orc.COL_1X16, orc.RHT | orc.SR, seed=0, offset=1)
+    del dY
+    gc.collect()
+    qXc = orc.quantize(X, orc.COL_1X16, orc.RHT, seed=0)
+    _check_sampled(nv, orc, "WGRAD 405B", qdYc, qXc)
+
+
+def _check_sampled(nv, orc, name, a, b):
+    A, B = H.upload(nv, a), H.upload(nv, b)
+    D = nv.nvfp4_gemm(A, B)
+    nv.check_device_errors()
+    m, n = _sample_positions(a["rows"], b["rows"])
+    ref = orc.gemm_fp64_sampled(a, b, m, n)
+    H.assert_gemm_close(H.host_f64(D[m, n]), ref, name)
+    del A, B, D

@@ -1,5 +1,7 @@
 """GPU parity of the quantisers against the CPU oracle: codes, MMA-layout
 scales (with padding), amax and s_dec bit for bit."""
+import functools
+
 import numpy as np
 import pytest
 
@@ -115,12 +117,21 @@ def test_quantize_llama8b_full(nv, orc, shape, kind, mode_name, spec):
     _run(nv, orc, _input(shape, kind, "bf16"), mode_name, spec, seed=0, offset=1)
 
 
-@pytest.mark.parametrize("mode_name,spec", [("ROW", 0), ("COL", "RHT|SR")])
-def test_quantize_32k_tokens_sampled(nv, orc, mode_name, spec):
-    """[32768, 14336]: the GPU quantises the whole tensor; the oracle computes
-    the tensor amax itself and quantises 128-row output slabs with it."""
-    R, Cn = 32768, 14336
-    x = syn.activations((R, Cn), seed=5)
+@functools.lru_cache(maxsize=2)
+def _activations_32k(R, Cn):
+    return syn.activations((R, Cn), seed=5)
+
+
+@pytest.mark.parametrize("R,Cn", [(32768, 14336), (32768, 4096)])
+@pytest.mark.parametrize("mode_name,spec", [("ROW", 0), ("ROW", "SR"), ("COL", "RHT|SR"),
+                                            ("BLK", "EMIT_T")])
+def test_quantize_32k_tokens_sampled(nv, orc, R, Cn, mode_name, spec):
+    """The quantiser-only sweep's 32k-token shapes: the GPU quantises the whole
+    tensor; the oracle computes the tensor amax itself and quantises sampled
+    128-row output slabs with it (each element's stochastic-rounding index
+    taken in the whole output), compared bit for bit: codes, the slab's scale
+    atoms and, for 16x16, its columns of the transposed codes."""
+    x = _activations_32k(R, Cn)
     mode, flags = _mode(orc, mode_name), _flags(orc, spec)
     q = nv.nvfp4_quantize(H.dev_bf16(x), _mode(nv, mode_name), _flags(nv, spec), seed=2, offset=4)
     amax = orc.amax(x, mode, flags & orc.RHT, seed=2)
@@ -128,17 +139,18 @@ def test_quantize_32k_tokens_sampled(nv, orc, mode_name, spec):
     orows, ocols = orc.out_shape(mode, R, Cn)
     codes = q.codes.cpu().numpy().reshape(orows, ocols // 2)
     scales = q.scales.cpu().numpy()
+    codes_t = q.codes_t.cpu().numpy().reshape(ocols, orows // 2) if flags & orc.EMIT_T else None
     atom_bytes = ((ocols // 16 + 3) // 4) * 512
     rng = np.random.Generator(np.random.PCG64(9))
-    for rb in sorted(set(rng.integers(0, orows // 128, 3).tolist()) | {orows // 128 - 1}):
+    for rb in sorted(set(rng.integers(0, orows // 128, 3).tolist()) | {0, orows // 128 - 1}):
         sl = slice(rb * 128, rb * 128 + 128)
-        xs = np.ascontiguousarray(x[sl] if mode == orc.ROW_1X16 else x[:, sl])
-        # the slab's own SR counters start at its first element: compare codes
-        # only for RNE; for SR compare the scales and the amax-derived s_dec
-        o = orc.quantize(xs, mode, flags & ~orc.SR, seed=2, offset=4, amax_given=float(amax))
-        assert np.array_equal(scales[rb * atom_bytes:(rb + 1) * atom_bytes], o["scales_sw"])
-        if not flags & orc.SR:
-            assert np.array_equal(codes[sl], o["codes"])
+        xs = np.ascontiguousarray(x[:, sl] if mode == orc.COL_1X16 else x[sl])
+        o = orc.quantize(xs, mode, flags, seed=2, offset=4, amax_given=float(amax),
+                         sr_index_base=rb * 128 * ocols)
+        assert np.array_equal(scales[rb * atom_bytes:(rb + 1) * atom_bytes], o["scales_sw"]), rb
+        assert np.array_equal(codes[sl], o["codes"]), rb
+        if codes_t is not None:
+            assert np.array_equal(codes_t[:, rb * 64:(rb + 1) * 64], o["codes_t"]), rb
 
 
 @pytest.mark.parametrize("shape,kind,dtype", [((336, 400), "dy", "bf16"), ((128, 256), "x", "fp32"),

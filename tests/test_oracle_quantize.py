@@ -215,3 +215,22 @@ def test_invalid_arguments_rejected(orc):
         orc.quantize(syn.activations((32, 32)), orc.BLOCK_16X16, orc.RHT)
     with pytest.raises(ValueError):
         orc.quantize(syn.activations((32, 32)), orc.ROW_1X16, orc.EMIT_T)
+
+
+def test_sr_window_equals_slab_of_whole(orc):
+    """Quantising a window of output rows with sr_index_base = first row x
+    output columns reproduces that window of the whole operand's SR codes
+    (row and transposing modes), given the whole operand's amax."""
+    x = syn.gradients((96, 64), seed=21)
+    for mode, flags in ((orc.ROW_1X16, orc.SR), (orc.COL_1X16, orc.SR | orc.RHT)):
+        whole = orc.quantize(x, mode, flags, seed=3, offset=5)
+        orows, ocols = orc.out_shape(mode, *x.shape)
+        r0, r1 = 16, 48
+        xs = x[r0:r1] if mode == orc.ROW_1X16 else x[:, r0:r1]
+        win = orc.quantize(np.ascontiguousarray(xs), mode, flags, seed=3, offset=5,
+                           amax_given=float(whole["amax"]), sr_index_base=r0 * ocols)
+        assert np.array_equal(win["codes"], whole["codes"][r0:r1])
+        # without the base the window draws other random words
+        other = orc.quantize(np.ascontiguousarray(xs), mode, flags, seed=3, offset=5,
+                             amax_given=float(whole["amax"]))
+        assert not np.array_equal(other["codes"], whole["codes"][r0:r1])
