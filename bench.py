@@ -56,6 +56,10 @@ def parse():
     p.add_argument("--n", type=int, default=14336)
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default="layer", choices=["layer", "mlp"],
+                   help="layer: the linear layer's step (default, the headline); mlp: the "
+                        "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336")
+    p.add_argument("--mlp-tokens", type=int, default=32768)
     return p.parse_args()
 
 
@@ -456,12 +460,88 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_mlp(args):
+    """The SwiGLU MLP (FP32 master weights quantised 16x16 every step, 9 NVFP4
+    GEMMs, WGRAD folded into FP32 master grads) forward + backward through
+    nvfp4_mlp_fwd / nvfp4_mlp_bwd; one JSON line, device-resident inputs,
+    L2 flushed between steps.  Not the headline metric."""
+    import torch
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    world, rank = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    M, D, F = args.mlp_tokens, 4096, 14336
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+
+    X = dev_bf16(syn.activations((M, D), seed=1))
+    dY = dev_bf16(syn.gradients((M, D), seed=3))
+    Wg, Wu = (torch.from_numpy(syn.weights((F, D), seed=s, master_fp32=True)).to(device)
+              for s in (4, 5))
+    Wd = torch.from_numpy(syn.weights((D, F), seed=6, master_fp32=True)).to(device)
+    sb, wb = nv.mlp_sizes(M, D, F)
+    saved = torch.empty(sb, dtype=torch.uint8, device=device)
+    ws = torch.empty(wb, dtype=torch.uint8, device=device)
+    Y = torch.empty(M, D, dtype=torch.bfloat16, device=device)
+    dX = torch.empty(M, D, dtype=torch.bfloat16, device=device)
+    gWg, gWu = (torch.zeros(F, D, dtype=torch.float32, device=device) for _ in range(2))
+    gWd = torch.zeros(D, F, dtype=torch.float32, device=device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.int32, device=device)
+
+    def step(i):
+        p = nv.mlp_params(M, D, F, Wg, Wu, Wd, seed=0, step=i, rht=True)
+        nv.nvfp4_mlp_fwd(p, X, Y, saved, ws)
+        nv.nvfp4_mlp_bwd(p, dY, saved, dX, gWg, gWu, gWd, ws)
+
+    for i in range(args.warmup):
+        flush.fill_(1)
+        flush_rd.amax()
+        step(i)
+    nv.check_device_errors()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        flush_rd.amax()
+        evs[i][0].record()
+        step(args.warmup + i)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    nv.check_device_errors()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), device) / args.steps
+    flops = 9 * 2.0 * M * D * F
+    if rank == 0:
+        print(json.dumps({
+            "metric": "NVFP4 SwiGLU MLP forward + backward TFLOP/s (9 GEMMs) on 1 GB300",
+            "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4", "data": DATA,
+            "config": {"workload": f"SwiGLU MLP fwd+bwd, tokens {M}, hidden {D}, ffn {F}, "
+                                   "FP32 master weights and grads",
+                       "l2": "flushed before every timed step (256 MiB write + read, untimed)"},
+            "impl": "ours"}), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "mlp":
+        run_mlp(args)
     else:
         run_ours(args)
 

@@ -99,6 +99,27 @@ bool dims_ok(int64_t M, int64_t D, int64_t F) {
     if (_s != NVFP4_OK) return _s;          \
   } while (0)
 
+// A bf16 operand [rows, cols] quantised twice -- row-wise (FPROP / DGRAD
+// operand) and column-wise (WGRAD operand) -- with both tensor amaxes taken
+// from one read of x; the two quantise passes then use them as given.
+nvfp4_status quantize_pair(const void* x, int64_t rows, int64_t cols, uint32_t row_flags,
+                           uint32_t col_flags, uint64_t seed, uint64_t row_offset,
+                           uint64_t col_offset, nvfp4_tensor* row, nvfp4_tensor* col, void* ws,
+                           size_t wsb, cudaStream_t st) {
+  const bool rht = col_flags & NVFP4_RHT;
+  NVFP4_TRY(amax_impl(x, NVFP4_IN_BF16, rows, cols, cols, seed, row->amax,
+                      rht ? col->amax : nullptr, ws, wsb, st));
+  if (!rht &&
+      cudaMemcpyAsync(col->amax, row->amax, sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_ROW_1X16,
+                          row_flags | NVFP4_AMAX_GIVEN, seed, row_offset, row, nullptr, 0, st));
+  NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_COL_1X16,
+                          col_flags | NVFP4_AMAX_GIVEN, seed, col_offset, col, nullptr, 0, st));
+  return NVFP4_OK;
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -144,17 +165,11 @@ nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, vo
                           &s.qWu, ws, wsb, st));
   NVFP4_TRY(quantize_impl(p->Wd, NVFP4_IN_FP32, D, F, F, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
                           &s.qWd, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(X, NVFP4_IN_BF16, M, D, D, NVFP4_ROW_1X16, 0, p->seed, 0, &w.qX, ws,
-                          wsb, st));
-  NVFP4_TRY(quantize_impl(X, NVFP4_IN_BF16, M, D, D, NVFP4_COL_1X16, rht, p->seed, 0, &s.qXc, ws,
-                          wsb, st));
+  NVFP4_TRY(quantize_pair(X, M, D, 0, rht, p->seed, 0, 0, &w.qX, &s.qXc, ws, wsb, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWg, 0, s.G, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWu, 0, s.U, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   NVFP4_TRY(swiglu_fwd_impl(s.G, s.U, w.H, M * F, st));
-  NVFP4_TRY(quantize_impl(w.H, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, 0, p->seed, 0, &w.qH, ws,
-                          wsb, st));
-  NVFP4_TRY(quantize_impl(w.H, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht, p->seed, 0, &s.qHc,
-                          ws, wsb, st));
+  NVFP4_TRY(quantize_pair(w.H, M, F, 0, rht, p->seed, 0, 0, &w.qH, &s.qHc, ws, wsb, st));
   NVFP4_TRY(gemm_impl(&w.qH, 0, &s.qWd, 0, Y, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
   return NVFP4_OK;
 }
@@ -185,23 +200,17 @@ nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void
   void* ws = w.partials;
   const size_t wsb = kQuantWorkspaceBytes;
 
-  NVFP4_TRY(quantize_impl(dY, NVFP4_IN_BF16, M, D, D, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 0,
-                          &w.qdY, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(dY, NVFP4_IN_BF16, M, D, D, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
-                          o + 1, &w.qdYc, ws, wsb, st));
+  NVFP4_TRY(quantize_pair(dY, M, D, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 0, o + 1, &w.qdY,
+                          &w.qdYc, ws, wsb, st));
   // DGRAD of the down projection: dH = dY . Wd  (Wd read through its transpose)
   NVFP4_TRY(gemm_impl(&w.qdY, 0, &s.qWd, 1, w.dH, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   // WGRAD of the down projection: dWd += dY^T . H
   NVFP4_TRY(gemm_impl(&w.qdYc, 0, &s.qHc, 0, dWd, NVFP4_D_F32_ACCUM, nullptr, D, F, M, 0, st));
   NVFP4_TRY(swiglu_bwd_impl(w.dH, s.G, s.U, w.dG, w.dU, M * F, st));
-  NVFP4_TRY(quantize_impl(w.dG, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 2,
-                          &w.qdG, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(w.dG, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
-                          o + 3, &w.qdGc, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(w.dU, NVFP4_IN_BF16, M, F, F, NVFP4_ROW_1X16, NVFP4_SR, p->seed, o + 4,
-                          &w.qdU, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(w.dU, NVFP4_IN_BF16, M, F, F, NVFP4_COL_1X16, rht | NVFP4_SR, p->seed,
-                          o + 5, &w.qdUc, ws, wsb, st));
+  NVFP4_TRY(quantize_pair(w.dG, M, F, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 2, o + 3, &w.qdG,
+                          &w.qdGc, ws, wsb, st));
+  NVFP4_TRY(quantize_pair(w.dU, M, F, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 4, o + 5, &w.qdU,
+                          &w.qdUc, ws, wsb, st));
   // DGRAD of gate and up: dX = dG . Wg + dU . Wu (second GEMM adds the first)
   NVFP4_TRY(gemm_impl(&w.qdG, 0, &s.qWg, 1, w.dXg, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
   NVFP4_TRY(gemm_impl(&w.qdU, 0, &s.qWu, 1, dX, NVFP4_D_BF16_ADD_C, w.dXg, M, D, F, 0, st));
