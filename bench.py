@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--n", type=int, default=14336)
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", default="layer", choices=["layer", "mlp"],
+    p.add_argument("--workload", default="layer", choices=["layer", "mlp", "rht_study"],
                    help="layer: the linear layer's step (default, the headline); mlp: the "
                         "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336")
     p.add_argument("--mlp-tokens", type=int, default=32768)
@@ -534,6 +534,52 @@ def run_mlp(args):
             "impl": "ours"}), flush=True)
 
 
+def run_rht_study(args):
+    """The recipe's two WGRAD modes compared on the outlier-laden synthetic
+    layer (M = 8192, K = 4096, N = 14336): dW = dY^T X through the NVFP4 path
+    with the RHT on both WGRAD operands (X^T RNE, dY^T SR) and without it
+    ("no_rht"), each against the exact product of the bf16 inputs, on 16384
+    sampled outputs (FP64).  Reported: relative RMS error and the largest
+    sampled error relative to rms(exact), per mode, for three SR seeds."""
+    import torch
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    M, K, N = args.m, args.k, args.n
+    X, _, dY = syn.linear_layer(M, K, N)
+    Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+    dYd = torch.from_numpy(dY.view(np.int16)).view(torch.bfloat16).cuda()
+    rng = np.random.Generator(np.random.PCG64(17))
+    n_idx = torch.from_numpy(rng.integers(0, N, 16384)).cuda()
+    k_idx = torch.from_numpy(rng.integers(0, K, 16384)).cuda()
+    # exact sampled dW[n, k] = sum_m dY[m, n] X[m, k] in FP64
+    exact = (dYd.double()[:, n_idx] * Xd.double()[:, k_idx]).sum(0)
+    rms = float(exact.pow(2).mean().sqrt())
+    out = {}
+    for mode in ("rht", "no_rht"):
+        flag = nv.RHT if mode == "rht" else 0
+        errs, worst = [], []
+        for seed in (0, 1, 2):
+            qdYc = nv.nvfp4_quantize(dYd, nv.COL_1X16, flag | nv.SR, seed=seed, offset=1)
+            qXc = nv.nvfp4_quantize(Xd, nv.COL_1X16, flag, seed=seed)
+            dW = nv.nvfp4_gemm(qdYc, qXc)
+            got = dW[n_idx, k_idx].double()
+            errs.append(float((got - exact).pow(2).mean().sqrt()) / rms)
+            worst.append(float((got - exact).abs().max()) / rms)
+        out[mode] = {"rel_rms_err": [round(e, 5) for e in errs],
+                     "max_err_over_rms": [round(w, 4) for w in worst]}
+    nv.check_device_errors()
+    print(json.dumps({"metric": "WGRAD relative error vs exact dY^T X, RHT vs no_rht",
+                      "unit": "relative", "higher_is_better": False, "n_gpus": 1,
+                      "config": {"workload": f"linear layer M={M} K={K} N={N}, synthetic "
+                                             "X with x50 outliers at rate 1e-3; 16384 sampled "
+                                             "outputs; SR seeds 0, 1, 2"},
+                      "data": DATA, "result": out, "impl": "ours"}), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3 and args.impl == "ours":
@@ -542,6 +588,8 @@ def main():
         run_reference(args)
     elif args.workload == "mlp":
         run_mlp(args)
+    elif args.workload == "rht_study":
+        run_rht_study(args)
     else:
         run_ours(args)
 
