@@ -313,6 +313,15 @@ NVFP4_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Relaxed arrive on an mbarrier of any CTA in the cluster: no release fence,
+// so it does not wait for the thread's earlier memory operations (bulk tensor
+// stores still in flight, for one).  For signals whose ordering is already
+// established otherwise, e.g. tensor-memory loads completed by
+// tcgen05.wait::ld and fenced by tcgen05.fence::before_thread_sync.
+NVFP4_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 NVFP4_DEV void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }

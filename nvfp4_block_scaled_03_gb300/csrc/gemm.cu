@@ -634,7 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      // the loads above have completed; a release here would also wait for
+      // this warp's tensor stores of the previous tile
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
       acc_ph ^= 1u;
       if (DMODE == NVFP4_D_BF16) {
         // each 32-column chunk: bf16 rows into a staging box (lane = row; the
