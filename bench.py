@@ -38,7 +38,7 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # M=8192, N=14336, K=4096, from one ncu capture of that launch
 # (dram__bytes_read.sum 53.2 MB + dram__bytes_write.sum 188.1 MB); None once
 # the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = 53.193472e6 + 188.105728e6
+FPROP_TRAFFIC_BYTES = 53.143552e6 + 187.872512e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
@@ -56,9 +56,13 @@ def parse():
     p.add_argument("--n", type=int, default=14336)
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", default="layer", choices=["layer", "mlp", "rht_study"],
+    p.add_argument("--workload", default="layer",
+                   choices=["layer", "mlp", "rht_study", "quant_sweep", "gemm_405b"],
                    help="layer: the linear layer's step (default, the headline); mlp: the "
-                        "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336")
+                        "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336; "
+                        "rht_study: WGRAD error with and without the RHT; quant_sweep: quantiser "
+                        "GB/s over four shapes and six forms; gemm_405b: the Llama-3.1-405B MLP "
+                        "projections' GEMMs")
     p.add_argument("--mlp-tokens", type=int, default=32768)
     return p.parse_args()
 
@@ -580,6 +584,185 @@ def run_rht_study(args):
                       "data": DATA, "result": out, "impl": "ours"}), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# further measurement runs: the quantiser sweep and the 405B GEMM shapes
+# ---------------------------------------------------------------------------
+def _timed(fn, reps, flush_l2):
+    """Mean and min device time (ms) of fn over reps calls, L2 flushed (untimed)
+    before each; CUDA events on the current stream."""
+    import torch
+    for _ in range(2):
+        flush_l2(1)
+        fn()
+    ts = []
+    for i in range(reps):
+        flush_l2(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.mean(ts), min(ts)
+
+
+def _flusher(device):
+    import torch
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.int32, device=device)
+
+    def flush_l2(v):
+        flush.fill_(v)
+        flush_rd.amax()
+    return flush_l2
+
+
+def run_quant_sweep(args):
+    """Quantiser throughput over the activation and gradient shapes of the
+    Llama-3-8B MLP ([8192 | 32768] tokens x [4096 | 14336]) in each form the
+    recipe uses: 1x16 RNE (activations), 1x16 SR (gradients), 1x16 along
+    columns with RHT (the WGRAD operands, RNE and SR), 1x16 RHT + SR along rows,
+    and 16x16 RNE with the transposed copy (weights).  Timed both as the full
+    call (amax pass + quantise pass) and as the quantise pass alone (amax
+    given); GB/s on algorithmic bytes (bf16 read once, codes and the unique
+    scale bytes written) against the HBM peak."""
+    import torch
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    peaks, peak_src = load_peaks()
+    flush_l2 = _flusher(device)
+    forms = [("row_rne", nv.ROW_1X16, 0), ("row_sr", nv.ROW_1X16, nv.SR),
+             ("row_rht_sr", nv.ROW_1X16, nv.RHT | nv.SR), ("col_rht_rne", nv.COL_1X16, nv.RHT),
+             ("col_rht_sr", nv.COL_1X16, nv.RHT | nv.SR),
+             ("blk16_rne_t", nv.BLOCK_16X16, nv.EMIT_T)]
+    reps = max(3, min(args.steps, 20))
+    results = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for rows, cols in ((8192, 4096), (8192, 14336), (32768, 4096), (32768, 14336)):
+        data = {}
+        for kind, gen in (("act", syn.activations), ("grad", syn.gradients)):
+            data[kind] = torch.from_numpy(gen((rows, cols)).view(np.int16)).view(
+                torch.bfloat16).to(device)
+        elts = rows * cols
+        ws = torch.empty(nv.quantize_sizes(rows, cols, nv.ROW_1X16)[3], dtype=torch.uint8,
+                         device=device)
+        for name, mode, flags in forms:
+            x = data["grad" if flags & nv.SR else "act"]
+            q = nv.alloc_qtensor(rows, cols, mode, flags, device=device)
+
+            def full():
+                nv.nvfp4_quantize(x, mode, flags, seed=0, offset=0, out=q, workspace=ws)
+
+            def given():
+                nv.nvfp4_quantize(x, mode, flags | nv.AMAX_GIVEN, seed=0, offset=0, out=q,
+                                  workspace=ws)
+            t_full, t_full_min = _timed(full, reps, flush_l2)   # also leaves q.amax set
+            t_q, t_q_min = _timed(given, reps, flush_l2)
+            t16 = mode == nv.BLOCK_16X16
+            nbytes = 2 * elts + (elts if t16 else elts / 2) + (2 * elts / 256 if t16 else elts / 16)
+            results.append({
+                "shape": [rows, cols], "form": name, "algorithmic_bytes": int(nbytes),
+                "ms_amax_and_quantise": round(t_full, 4), "ms_quantise": round(t_q, 4),
+                "gbs_amax_and_quantise": round(nbytes / (t_full * 1e-3) / 1e9, 1),
+                "gbs_quantise": round(nbytes / (t_q * 1e-3) / 1e9, 1),
+                "frac_quantise": round(nbytes / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "ms_quantise_min": round(t_q_min, 4)})
+            del q
+        del data, ws
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    nv.check_device_errors()
+    print(json.dumps({
+        "metric": "NVFP4 quantiser GB/s on algorithmic bytes", "unit": "GB/s",
+        "higher_is_better": True, "n_gpus": 1, "dtype": "bf16 in, nvfp4 out", "data": DATA,
+        "config": {"workload": "quantiser sweep: tokens {8192, 32768} x {4096, 14336}, six "
+                               "quantiser forms",
+                   "reps": reps, "l2": "flushed before every timed call (untimed)"},
+        "peak_gbs": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+        "results": results, "clocks": clk, "impl": "ours"}), flush=True)
+
+
+def run_gemm_405b(args):
+    """The Llama-3.1-405B MLP up projection (X [8192, 16384], W_up [53248,
+    16384]) and down projection (H [8192, 53248], W_down [16384, 53248]): the
+    FPROP, DGRAD and WGRAD GEMMs of each on operands quantised in the recipe's
+    forms outside the timed region, L2 flushed before every timed GEMM.
+    TFLOP/s and the fraction of the FP4 peak per GEMM.  Inputs come from
+    seeded torch CUDA generators with the synthetic recipe's distributions
+    (generating 2.9e9 values on the host would take minutes)."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    flush_l2 = _flusher(device)
+    gen = torch.Generator(device=device)
+
+    def normal(shape, seed, sigma, outliers=False):
+        gen.manual_seed(seed)
+        x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * sigma
+        if outliers:
+            x = torch.where(torch.rand(shape, generator=gen, device=device) < 1e-3, x * 50, x)
+        return x.to(torch.bfloat16)
+
+    reps = max(3, min(args.steps, 10))
+    results = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for proj, (M, K, N), seeds in (("up", (8192, 16384, 53248), (1, 2, 3)),
+                                   ("down", (8192, 53248, 16384), (11, 12, 13))):
+        X = normal((M, K), seeds[0], 1.0, outliers=True)
+        W = normal((N, K), seeds[1], 0.02)
+        dY = normal((M, N), seeds[2], 1e-3)
+        qX = nv.nvfp4_quantize(X, nv.ROW_1X16)
+        qXc = nv.nvfp4_quantize(X, nv.COL_1X16, nv.RHT, seed=0)
+        qW = nv.nvfp4_quantize(W, nv.BLOCK_16X16, nv.EMIT_T)
+        qdY = nv.nvfp4_quantize(dY, nv.ROW_1X16, nv.SR, seed=0, offset=0)
+        qdYc = nv.nvfp4_quantize(dY, nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1)
+        del X, W, dY
+        out = {"fprop": torch.empty(M, N, dtype=torch.bfloat16, device=device),
+               "dgrad": torch.empty(M, K, dtype=torch.bfloat16, device=device),
+               "wgrad": torch.empty(N, K, dtype=torch.bfloat16, device=device)}
+        calls = {"fprop": lambda: nv.nvfp4_gemm(qX, qW, out=out["fprop"]),
+                 "dgrad": lambda: nv.nvfp4_gemm(qdY, qW, b_view=1, out=out["dgrad"]),
+                 "wgrad": lambda: nv.nvfp4_gemm(qdYc, qXc, out=out["wgrad"])}
+        for g, fn in calls.items():
+            ms, ms_min = _timed(fn, reps, flush_l2)
+            tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+            results.append({"projection": proj, "gemm": g, "M": M, "N": N, "K": K,
+                            "shape_MxNxK": {"fprop": [M, N, K], "dgrad": [M, K, N],
+                                            "wgrad": [N, K, M]}[g],
+                            "ms": round(ms, 4), "ms_min": round(ms_min, 4),
+                            "tflops": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4)})
+        del qX, qXc, qW, qdY, qdYc, out, calls
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    nv.check_device_errors()
+    flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in results)
+    ms_all = sum(r["ms"] for r in results)
+    print(json.dumps({
+        "metric": "NVFP4 GEMM TFLOP/s, Llama-3.1-405B MLP up and down projections (6 GEMMs)",
+        "value": round(flops / (ms_all * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+        "higher_is_better": True, "n_gpus": 1, "dtype": "nvfp4",
+        "data": "synthetic, seeded torch CUDA generators: X, H ~ N(0,1) with x50 outliers at "
+                "rate 1e-3, W ~ N(0,0.02), dY ~ N(0,1e-3), bf16",
+        "config": {"workload": "Llama-3.1-405B MLP: up [8192,16384]x[53248,16384]^T, down "
+                               "[8192,53248]x[16384,53248]^T; FPROP, DGRAD, WGRAD each",
+                   "reps": reps, "l2": "flushed before every timed GEMM (untimed)"},
+        "peak_tflops": round(fp4_peak, 1),
+        "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)",
+        "results": results, "clocks": clk, "impl": "ours"}), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3 and args.impl == "ours":
@@ -590,6 +773,10 @@ def main():
         run_mlp(args)
     elif args.workload == "rht_study":
         run_rht_study(args)
+    elif args.workload == "quant_sweep":
+        run_quant_sweep(args)
+    elif args.workload == "gemm_405b":
+        run_gemm_405b(args)
     else:
         run_ours(args)
 
