@@ -30,6 +30,8 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libnvfp4_oracle.so")
 
 ROW_1X16, COL_1X16, BLOCK_16X16 = 0, 1, 2
+MXFP4, MXFP8 = 0, 1
+MX_ROW, MX_COL = 0, 1
 RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
 IN_BF16, IN_FP32 = 0, 1
 
@@ -87,6 +89,11 @@ def lib():
                 "orc_gemm_fp64": ([vp, vp, f32, vp, vp, f32, i64, i64, i64, vp], None),
                 "orc_gemm_fp64_sampled": ([vp, vp, f32, vp, vp, f32, i64, vp, vp, i64, vp],
                                           None),
+                "orc_e8m0_value": ([C.c_uint8], f32),
+                "orc_e8m0_scale": ([f32, C.c_int], C.c_uint8),
+                "orc_mx_quantize": ([vp, C.c_int, i64, i64, i64, C.c_int, C.c_int, vp, vp],
+                                    C.c_int),
+                "orc_mx_dequant": ([vp, vp, C.c_int, i64, i64, vp], None),
                 "orc_swiglu_fwd": ([vp, vp, i64, vp], None),
                 "orc_swiglu_bwd": ([vp, vp, vp, i64, vp, vp], None),
             }
@@ -271,6 +278,48 @@ def gemm_fp64_sampled(qa: dict, qb: dict, m_idx, n_idx) -> np.ndarray:
     lib().orc_gemm_fp64_sampled(_p(qa["codes"]), _p(qa["scales"]), float(qa["s_dec"]),
                                 _p(qb["codes"]), _p(qb["scales"]), float(qb["s_dec"]),
                                 qa["cols"], _p(m_idx), _p(n_idx), len(m_idx), _p(out))
+    return out
+
+
+# ---- MX comparison formats (OCP Microscaling: 32-element blocks, E8M0) --------
+def e8m0_value(b: int) -> float:
+    return float(lib().orc_e8m0_value(b))
+
+
+def e8m0_scale(amax: float, fmt: int) -> int:
+    return int(lib().orc_e8m0_scale(amax, fmt))
+
+
+def mx_quantize(x: np.ndarray, mode: int, fmt: int) -> dict:
+    """MXFP4 / MXFP8 quantisation of a 2-D bf16 (uint16 bits) or float32
+    array: 32-element blocks along the output's rows (``MX_ROW``: along the
+    input's columns; ``MX_COL``: along its rows, output transposed).  Returns
+    ``codes`` ([orows, ocols/2] packed E2M1 or [orows, ocols] E4M3),
+    ``scales`` ([orows, ocols/32] E8M0), ``rows``/``cols`` (output shape)."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        dt = IN_BF16
+    elif x.dtype == np.float32:
+        dt = IN_FP32
+    else:
+        raise TypeError(f"oracle mx_quantize takes bf16 bits (uint16) or float32, got {x.dtype}")
+    rows, cols = x.shape
+    orows, ocols = (cols, rows) if mode == MX_COL else (rows, cols)
+    if ocols % 32:
+        raise ValueError("blocked dimension must be a multiple of 32")
+    codes = np.zeros((orows, ocols // 2 if fmt == MXFP4 else ocols), np.uint8)
+    scales = np.zeros((orows, ocols // 32), np.uint8)
+    rc = lib().orc_mx_quantize(_p(x), dt, rows, cols, cols, mode, fmt, _p(codes), _p(scales))
+    if rc != 0:
+        raise ValueError(f"oracle mx_quantize rejected its arguments (rc={rc})")
+    return {"codes": codes, "scales": scales, "rows": orows, "cols": ocols, "fmt": fmt,
+            "mode": mode}
+
+
+def mx_dequant(q: dict) -> np.ndarray:
+    out = np.zeros((q["rows"], q["cols"]), np.float64)
+    lib().orc_mx_dequant(_p(q["codes"]), _p(q["scales"]), q["fmt"], q["rows"], q["cols"],
+                         _p(out))
     return out
 
 

@@ -492,3 +492,105 @@ void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, in
     dg[i] = orc_bf16_from_double(d * uv * s * (1.0 + gv * (1.0 - s)));
   }
 }
+
+/* ======================================================================== */
+/* MX comparison formats ("NVFP4 pretraining recipe" page, "NVFP4 format
+ * and advantages": MXFP4 takes 32-element blocks and power-of-two E8M0
+ * scales, against NVFP4's 16-element E4M3 blocks; the Triton-on-Blackwell
+ * quote: MXFP8 and MXFP4 block-scaled GEMMs).  The pages link the OCP
+ * Microscaling specification for the formats; its conversion is restated
+ * here: the block's shared exponent is floor(log2(amax)) minus the largest
+ * normal exponent of the element format (2 for E2M1, 8 for E4M3), clamped
+ * to the E8M0 range [-127, 127]; each element is v / 2^shared rounded to
+ * nearest-even and saturated to the element format's largest finite value.
+ * Readings (the spec leaves them to the implementation): an all-zero block
+ * gets scale byte 0 and zero codes; a block whose amax is not finite gets
+ * scale byte 0xFF (the E8M0 NaN) and zero codes; negative values that round
+ * to zero keep their sign (E2M1 code 0x8, E4M3 byte 0x80).                 */
+/* ======================================================================== */
+float orc_e8m0_value(uint8_t b) {
+  if (b == 0xFF) return NAN;
+  return ldexpf(1.0f, (int)b - 127);
+}
+
+/* floor(log2(a)) of a positive finite float, from frexp (exact). */
+static int floor_log2f(float a) {
+  int e;
+  (void)frexpf(a, &e);  /* a = m 2^e, m in [0.5, 1) */
+  return e - 1;
+}
+
+uint8_t orc_e8m0_scale(float amax, int fmt) {
+  if (!isfinite(amax)) return 0xFF;
+  if (amax == 0.0f) return 0;
+  const int emax = fmt == ORC_MXFP8 ? 8 : 2;
+  int shared = floor_log2f(amax) - emax;
+  if (shared < -127) shared = -127;
+  if (shared > 127) shared = 127;
+  return (uint8_t)(shared + 127);
+}
+
+void orc_mx_out_shape(int mode, int64_t rows, int64_t cols, int64_t* orows, int64_t* ocols) {
+  orc_out_shape(mode == ORC_MX_COL ? ORC_COL_1X16 : ORC_ROW_1X16, rows, cols, orows, ocols);
+}
+
+int orc_mx_quantize(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                    int mode, int fmt, uint8_t* codes, uint8_t* scales) {
+  if ((in_dtype != ORC_IN_BF16 && in_dtype != ORC_IN_FP32) || rows <= 0 || cols <= 0 ||
+      ld < cols || (mode != ORC_MX_ROW && mode != ORC_MX_COL) ||
+      (fmt != ORC_MXFP4 && fmt != ORC_MXFP8))
+    return 1;
+  if ((mode == ORC_MX_ROW && cols % 32) || (mode == ORC_MX_COL && rows % 32)) return 1;
+  int64_t orows, ocols;
+  orc_mx_out_shape(mode, rows, cols, &orows, &ocols);
+  const int64_t cbytes = fmt == ORC_MXFP4 ? ocols / 2 : ocols;
+  float v[32];
+  for (int64_t r = 0; r < orows; ++r) {
+    for (int64_t b = 0; b < ocols / 32; ++b) {
+      float a = 0.0f;
+      int nonfinite = 0;
+      for (int i = 0; i < 32; ++i) {
+        const int64_t c = b * 32 + i;   /* output column */
+        const int64_t idx = mode == ORC_MX_ROW ? r * ld + c : c * ld + r;
+        v[i] = load_in(x, in_dtype, idx);
+        if (!isfinite(v[i])) nonfinite = 1;
+        else if (fabsf(v[i]) > a) a = fabsf(v[i]);
+      }
+      const uint8_t sb = orc_e8m0_scale(nonfinite ? INFINITY : a, fmt);
+      scales[r * (ocols / 32) + b] = sb;
+      uint8_t* row = codes + r * cbytes;
+      for (int i = 0; i < 32; ++i) {
+        const int64_t c = b * 32 + i;
+        uint8_t code = 0;
+        if (sb != 0xFF && a != 0.0f) {
+          /* v / 2^shared: exact in FP64, then to float (only values far below
+           * the element format's smallest step can round there) */
+          const float y = (float)ldexp((double)v[i], -((int)sb - 127));
+          code = fmt == ORC_MXFP4 ? orc_e2m1_rne(y) : orc_e4m3_rne_sat(y);
+        } else if (sb != 0xFF && signbit(v[i])) {
+          code = fmt == ORC_MXFP4 ? 0x8 : 0x80;  /* -0 in an all-zero block */
+        }
+        if (fmt == ORC_MXFP4) put_code(row, c, code);
+        else row[c] = code;
+      }
+    }
+  }
+  return 0;
+}
+
+void orc_mx_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int64_t rows,
+                    int64_t cols, double* out) {
+  const int64_t cbytes = fmt == ORC_MXFP4 ? cols / 2 : cols;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const uint8_t sb = scales[r * (cols / 32) + c / 32];
+      double e;
+      if (fmt == ORC_MXFP4) {
+        const uint8_t byte = codes[r * cbytes + c / 2];
+        e = orc_e2m1_value((uint8_t)((c & 1) ? byte >> 4 : byte & 15));
+      } else {
+        e = orc_e4m3_value(codes[r * cbytes + c]);
+      }
+      out[r * cols + c] = e * (double)orc_e8m0_value(sb);
+    }
+}

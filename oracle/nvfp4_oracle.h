@@ -98,6 +98,20 @@ void orc_gemm_fp64_sampled(const uint8_t* codes_a, const uint8_t* scales_a, floa
                            int64_t K, const int64_t* m_idx, const int64_t* n_idx,
                            int64_t n_samples, double* out);
 
+/* ---- MX comparison formats (OCP Microscaling): 32-element blocks, E8M0 -- */
+enum { ORC_MXFP4 = 0, ORC_MXFP8 = 1 };
+enum { ORC_MX_ROW = 0, ORC_MX_COL = 1 };  /* blocks along the output's rows  */
+float   orc_e8m0_value(uint8_t b);               /* 2^(b-127); 0xFF is NaN    */
+uint8_t orc_e8m0_scale(float amax, int fmt);     /* a block's scale byte      */
+void    orc_mx_out_shape(int mode, int64_t rows, int64_t cols, int64_t* orows, int64_t* ocols);
+/* codes: MXFP4 [orows][ocols/2] packed like NVFP4, MXFP8 [orows][ocols] E4M3;
+ * scales: [orows][ocols/32] E8M0, row-major.  Returns 0, or nonzero on an
+ * invalid argument (the blocked dimension must be a multiple of 32). */
+int  orc_mx_quantize(const void* x, int in_dtype, int64_t rows, int64_t cols, int64_t ld,
+                     int mode, int fmt, uint8_t* codes, uint8_t* scales);
+void orc_mx_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int64_t rows,
+                    int64_t cols, double* out);
+
 /* ---- SwiGLU (between the MLP GEMMs) -------------------------------------- */
 void orc_swiglu_fwd(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h);
 void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, int64_t n,
