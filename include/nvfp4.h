@@ -191,6 +191,48 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t in_dtype, int64_t row
                                     uint64_t offset, nvfp4_tensor* out, nvfp4_stream stream);
 
 /* ---------------------------------------------------------------------- */
+/* MX comparison formats                                                   */
+/* ---------------------------------------------------------------------- */
+/* "NVFP4 pretraining recipe" page, "NVFP4 format and advantages": MXFP4
+ * scales 32-element blocks by powers of two (E8M0), against NVFP4's 16-element
+ * E4M3 blocks under a per-tensor scale; the same page quotes MXFP8 and MXFP4
+ * block-scaled GEMMs on Blackwell.  These quantisers produce those formats
+ * for comparison with NVFP4 (error studies), following the OCP Microscaling
+ * specification the page links. */
+typedef enum { NVFP4_MXFP4 = 0, NVFP4_MXFP8 = 1 } nvfp4_mx_format;
+enum {
+  NVFP4_MX_ROW = 0,  /* blocks of 32 along the columns; output [rows, cols]            */
+  NVFP4_MX_COL = 1   /* blocks of 32 along the rows; output transposed [cols, rows]    */
+};
+
+/* Byte sizes of the outputs of nvfp4_mx_quantize for x [rows, cols]:
+ * codes = out_rows * out_cols / 2 (MXFP4) or out_rows * out_cols (MXFP8),
+ * scales = out_rows * out_cols / 32.  Either pointer may be NULL.  Returns
+ * NVFP4_ERR_SHAPE unless the blocked dimension is a multiple of 32 (and, for
+ * NVFP4_MX_COL, cols a multiple of 8). */
+nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
+                            size_t* codes_bytes, size_t* scales_bytes);
+
+/* MXFP4 / MXFP8 quantisation of x [rows, cols] (bf16 or fp32, row-major,
+ * leading dim ld elements).  Per block of 32 consecutive output elements:
+ *   shared = clamp(floor(log2(amax)) - emax, -127, 127), emax = 2 (E2M1) or
+ *            8 (E4M3); scale byte = shared + 127 (E8M0, value 2^shared);
+ *            0 when the block is all zero; 0xFF (NaN) when it holds a value
+ *            that is not finite, with zero codes;
+ *   element = v / 2^shared rounded to nearest-even and saturated to the
+ *            element format's largest finite value (6 or 448), sign kept.
+ * Outputs (device, caller-owned, sizes from nvfp4_mx_sizes): codes row-major
+ * [out_rows][out_cols] -- MXFP4 packed two per byte, element 2i in the low
+ * nibble of byte i; MXFP8 one E4M3 byte each -- and scales row-major
+ * [out_rows][out_cols / 32].  x and codes must be 16-byte aligned and
+ * ld * element size a multiple of 16 bytes.  One kernel launch on `stream`;
+ * nothing is allocated.  Returns NVFP4_ERR_INVALID_ARG, _SHAPE, _ALIGN,
+ * _ARCH, _CUDA. */
+nvfp4_status nvfp4_mx_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                               int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
+                               nvfp4_stream stream);
+
+/* ---------------------------------------------------------------------- */
 /* Block-scaled GEMM                                                       */
 /* ---------------------------------------------------------------------- */
 /* Output modes of nvfp4_gemm. */

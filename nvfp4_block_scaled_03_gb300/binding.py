@@ -23,6 +23,8 @@ IN_BF16, IN_FP32 = 0, 1
 ROW_1X16, COL_1X16, BLOCK_16X16 = 0, 1, 2
 RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
 D_BF16, D_F32_ACCUM, D_BF16_ADD_C = 0, 1, 2
+MXFP4, MXFP8 = 0, 1
+MX_ROW, MX_COL = 0, 1
 TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256, TILE_128X256_MC2, TILE_128X256_K128 = \
     0, 1, 2, 3, 4, 5
 
@@ -70,6 +72,8 @@ def _load():
                        C.c_int),
         "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
                           C.c_int),
+        "nvfp4_mx_sizes": ([i64, i64, i32, i32, P(sz), P(sz)], C.c_int),
+        "nvfp4_mx_quantize": ([vp, i32, i64, i64, i64, i32, i32, vp, vp, vp], C.c_int),
         "nvfp4_mlp_sizes": ([i64, i64, i64, P(sz), P(sz)], C.c_int),
         "nvfp4_mlp_fwd": ([P(MlpParams), vp, vp, vp, sz, vp, sz, vp], C.c_int),
         "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
@@ -225,6 +229,37 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int, flags: int = 0, seed: int
                                       offset, C.byref(out.desc), _stream(stream)),
            "nvfp4_quantize_noalloc")
     return out
+
+
+def mx_sizes(rows, cols, mode, fmt):
+    c, s = C.c_size_t(), C.c_size_t()
+    _check(lib.nvfp4_mx_sizes(rows, cols, mode, fmt, C.byref(c), C.byref(s)), "nvfp4_mx_sizes")
+    return c.value, s.value
+
+
+def nvfp4_mx_quantize(x: torch.Tensor, mode: int, fmt: int, codes: torch.Tensor | None = None,
+                      scales: torch.Tensor | None = None, stream=None):
+    """MXFP4 / MXFP8 quantisation of a 2-D bf16/fp32 CUDA tensor (see
+    nvfp4_mx_quantize in nvfp4.h); returns (codes, scales) as uint8 tensors
+    shaped [out_rows, out_cols/2 or out_cols] and [out_rows, out_cols/32]."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    dt = {torch.bfloat16: IN_BF16, torch.float32: IN_FP32}.get(x.dtype)
+    if dt is None:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    rows, cols = x.shape
+    orows, ocols = (cols, rows) if mode == MX_COL else (rows, cols)
+    cb, sb = mx_sizes(rows, cols, mode, fmt)
+    if codes is None:
+        codes = torch.empty(orows, cb // orows, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(orows, sb // orows, dtype=torch.uint8, device=x.device)
+    if codes.numel() < cb or scales.numel() < sb:
+        raise ValueError("output buffers are smaller than nvfp4_mx_sizes gives")
+    _check(lib.nvfp4_mx_quantize(x.data_ptr(), dt, rows, cols, x.stride(0), mode, fmt,
+                                 codes.data_ptr(), scales.data_ptr(), _stream(stream)),
+           "nvfp4_mx_quantize")
+    return codes, scales
 
 
 def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,

@@ -103,6 +103,18 @@ nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t c
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
+                            size_t* codes_bytes, size_t* scales_bytes) {
+  return mx_sizes_impl(rows, cols, mode, fmt, codes_bytes, scales_bytes);
+}
+
+nvfp4_status nvfp4_mx_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                               int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
+                               nvfp4_stream stream) {
+  return mx_quantize_impl(x, in_dtype, rows, cols, ld, mode, fmt, codes, scales,
+                          static_cast<cudaStream_t>(stream));
+}
+
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                         int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
                         int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
