@@ -57,12 +57,14 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="layer",
-                   choices=["layer", "mlp", "rht_study", "quant_sweep", "gemm_405b"],
+                   choices=["layer", "mlp", "rht_study", "quant_sweep", "gemm_405b",
+                            "format_study"],
                    help="layer: the linear layer's step (default, the headline); mlp: the "
                         "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336; "
                         "rht_study: WGRAD error with and without the RHT; quant_sweep: quantiser "
                         "GB/s over four shapes and six forms; gemm_405b: the Llama-3.1-405B MLP "
-                        "projections' GEMMs")
+                        "projections' GEMMs; format_study: NVFP4 against MXFP4 and MXFP8 on the "
+                        "405B up projection's operands")
     p.add_argument("--mlp-tokens", type=int, default=32768)
     return p.parse_args()
 
@@ -763,6 +765,136 @@ def run_gemm_405b(args):
         "results": results, "clocks": clk, "impl": "ours"}), flush=True)
 
 
+def run_format_study(args):
+    """NVFP4 against the MX formats the page compares it with (MXFP4: 32-element
+    blocks, E8M0 scales; MXFP8 likewise with E4M3 elements) on the
+    Llama-3.1-405B MLP up projection's operands (X [8192, 16384] with x50
+    outliers at rate 1e-3, W [53248, 16384]): element-wise relative MSE of each
+    quantised operand, and the FPROP error on 16384 sampled outputs against the
+    exact product of the bf16 inputs -- NVFP4 through nvfp4_gemm (BF16 out),
+    the MX formats as the exact FP64 product of their dequantised operands (the
+    value an MX GEMM accumulates before rounding).  Plus the GB/s of the MX
+    quantisers.  Dequantisation here is measurement code (torch lookups)."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    peaks, peak_src = load_peaks()
+    M, K, N = 8192, 16384, 53248
+    gen = torch.Generator(device=device)
+
+    def normal(shape, seed, sigma, outliers=False):
+        gen.manual_seed(seed)
+        x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * sigma
+        if outliers:
+            x = torch.where(torch.rand(shape, generator=gen, device=device) < 1e-3, x * 50, x)
+        return x.to(torch.bfloat16)
+
+    X = normal((M, K), 1, 1.0, outliers=True)
+    W = normal((N, K), 2, 0.02)
+    e2m1 = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6],
+                        dtype=torch.float64, device=device)
+    e4m3 = torch.zeros(256, dtype=torch.float64, device=device)
+    for b in range(256):
+        s, e, m = b >> 7, (b >> 3) & 15, b & 7
+        v = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        e4m3[b] = float("nan") if (e == 15 and m == 7) else (-v if s else v)
+
+    def unpack4(codes, rows, cols):
+        c = codes.view(rows, cols // 2).long()
+        return torch.stack((c & 15, c >> 4), dim=-1).reshape(rows, cols)
+
+    def deq_nvfp4(q, rows, cols, r_idx):
+        """Rows r_idx of an NVFP4 operand (MMA-layout scales) in FP64."""
+        codes = q.codes.view(rows, cols // 2)[r_idx]
+        vals = e2m1[unpack4(codes, len(r_idx), cols)]
+        pc4 = ((cols // 16) + 3) // 4 * 4
+        r = r_idx.view(-1, 1)
+        c16 = torch.arange(cols // 16, device=device).view(1, -1)
+        off = ((r >> 7) * (pc4 >> 2) + (c16 >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 \
+            + (c16 & 3)
+        sc = e4m3[q.scales.long()[off]]
+        return vals * sc.repeat_interleave(16, dim=1) * float(q.s_dec.item())
+
+    def deq_mx(codes, scales, fmt, rows, cols, r_idx):
+        c = codes[r_idx]
+        vals = e2m1[unpack4(c, len(r_idx), cols)] if fmt == nv.MXFP4 else e4m3[c.long()]
+        sc = torch.exp2(scales[r_idx].double() - 127)
+        return vals * sc.repeat_interleave(32, dim=1)
+
+    results = {}
+    # element-wise error on row slabs (the whole operands, 4096 rows at a time)
+    qX = nv.nvfp4_quantize(X, nv.ROW_1X16)
+    qW = nv.nvfp4_quantize(W, nv.BLOCK_16X16, nv.EMIT_T)
+    mx = {f: (nv.nvfp4_mx_quantize(X, nv.MX_ROW, f), nv.nvfp4_mx_quantize(W, nv.MX_ROW, f))
+          for f in (nv.MXFP4, nv.MXFP8)}
+    torch.cuda.synchronize()
+    for name, T, rows in (("X", X, M), ("W", W, N)):
+        num = {"nvfp4": 0.0, "mxfp4": 0.0, "mxfp8": 0.0}
+        den = 0.0
+        for r0 in range(0, rows, 4096):
+            r_idx = torch.arange(r0, min(rows, r0 + 4096), device=device)
+            ref = T[r_idx].double()
+            den += float(ref.pow(2).sum())
+            q = qX if name == "X" else qW
+            num["nvfp4"] += float((deq_nvfp4(q, rows, K, r_idx) - ref).pow(2).sum())
+            for f, key in ((nv.MXFP4, "mxfp4"), (nv.MXFP8, "mxfp8")):
+                codes, scales = mx[f][0 if name == "X" else 1]
+                num[key] += float((deq_mx(codes, scales, f, rows, K, r_idx) - ref).pow(2).sum())
+        results[f"rel_mse_{name}"] = {k: round(v / den, 7) for k, v in num.items()}
+    # FPROP on sampled outputs
+    rng = np.random.Generator(np.random.PCG64(17))
+    m_idx = torch.from_numpy(rng.integers(0, M, 16384)).to(device)
+    n_idx = torch.from_numpy(rng.integers(0, N, 16384)).to(device)
+    exact = (X[m_idx].double() * W[n_idx].double()).sum(1)
+    rms = float(exact.pow(2).mean().sqrt())
+    Y = nv.nvfp4_gemm(qX, qW)
+    got = {"nvfp4": Y[m_idx, n_idx].double()}
+    for f, key in ((nv.MXFP4, "mxfp4"), (nv.MXFP8, "mxfp8")):
+        (xc, xs), (wc, ws) = mx[f]
+        got[key] = (deq_mx(xc, xs, f, M, K, m_idx) * deq_mx(wc, ws, f, N, K, n_idx)).sum(1)
+    results["fprop_sampled"] = {
+        k: {"rel_rms_err": round(float((v - exact).pow(2).mean().sqrt()) / rms, 6),
+            "max_err_over_rms": round(float((v - exact).abs().max()) / rms, 5)}
+        for k, v in got.items()}
+    del Y
+    # MX quantiser throughput (L2 flushed before each call)
+    flush_l2 = _flusher(device)
+    thr = {}
+    for name, T, rows in (("X", X, M), ("W", W, N)):
+        for f, key in ((nv.MXFP4, "mxfp4"), (nv.MXFP8, "mxfp8")):
+            codes, scales = mx[f][0 if name == "X" else 1]
+            for mode, mname in ((nv.MX_ROW, "row"), (nv.MX_COL, "col")):
+                if mode == nv.MX_COL:
+                    cb, sb = nv.mx_sizes(rows, K, mode, f)
+                    c_out = torch.empty(cb, dtype=torch.uint8, device=device)
+                    s_out = torch.empty(sb, dtype=torch.uint8, device=device)
+                else:
+                    c_out, s_out = codes, scales
+                ms, _ = _timed(lambda: nv.nvfp4_mx_quantize(T, mode, f, c_out, s_out), 5,
+                               flush_l2)
+                elts = rows * K
+                nbytes = 2 * elts + (elts / 2 if f == nv.MXFP4 else elts) + elts / 32
+                thr[f"{key}_{mname}_{name}"] = {
+                    "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    results["mx_quantiser_throughput"] = thr
+    nv.check_device_errors()
+    print(json.dumps({
+        "metric": "NVFP4 vs MXFP4 vs MXFP8: quantisation error and FPROP error",
+        "unit": "relative", "higher_is_better": False, "n_gpus": 1,
+        "config": {"workload": "Llama-3.1-405B MLP up projection operands: X [8192, 16384], "
+                               "W [53248, 16384]; FPROP on 16384 sampled outputs",
+                   "forms": "NVFP4: X 1x16 RNE, W 16x16 RNE (E4M3 block scales, FP32 tensor "
+                            "scale); MXFP4 / MXFP8: 1x32 RNE, E8M0 block scales",
+                   "peak_source": f"{peak_src} HBM copy"},
+        "data": "synthetic, seeded torch CUDA generators: X ~ N(0,1) with x50 outliers at "
+                "rate 1e-3, W ~ N(0,0.02), bf16",
+        "result": results, "impl": "ours"}), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3 and args.impl == "ours":
@@ -777,6 +909,8 @@ def main():
         run_quant_sweep(args)
     elif args.workload == "gemm_405b":
         run_gemm_405b(args)
+    elif args.workload == "format_study":
+        run_format_study(args)
     else:
         run_ours(args)
 
