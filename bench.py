@@ -868,7 +868,7 @@ def run_format_study(args):
             codes, scales = mx[f][0 if name == "X" else 1]
             for mode, mname in ((nv.MX_ROW, "row"), (nv.MX_COL, "col")):
                 if mode == nv.MX_COL:
-                    cb, sb = nv.mx_sizes(rows, K, mode, f)
+                    cb, sb, _ = nv.mx_sizes(rows, K, mode, f)
                     c_out = torch.empty(cb, dtype=torch.uint8, device=device)
                     s_out = torch.empty(sb, dtype=torch.uint8, device=device)
                 else:

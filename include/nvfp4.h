@@ -207,11 +207,13 @@ enum {
 
 /* Byte sizes of the outputs of nvfp4_mx_quantize for x [rows, cols]:
  * codes = out_rows * out_cols / 2 (MXFP4) or out_rows * out_cols (MXFP8),
- * scales = out_rows * out_cols / 32.  Either pointer may be NULL.  Returns
+ * scales = out_rows * out_cols / 32, scales_sw = the same scales in the MMA
+ * layout (512-byte atoms of 128 rows x 4 scale columns, rows padded to 128
+ * and scale columns to 4).  Any pointer may be NULL.  Returns
  * NVFP4_ERR_SHAPE unless the blocked dimension is a multiple of 32 (and, for
  * NVFP4_MX_COL, cols a multiple of 8). */
 nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
-                            size_t* codes_bytes, size_t* scales_bytes);
+                            size_t* codes_bytes, size_t* scales_bytes, size_t* scales_sw_bytes);
 
 /* MXFP4 / MXFP8 quantisation of x [rows, cols] (bf16 or fp32, row-major,
  * leading dim ld elements).  Per block of 32 consecutive output elements:
@@ -224,13 +226,32 @@ nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fm
  * Outputs (device, caller-owned, sizes from nvfp4_mx_sizes): codes row-major
  * [out_rows][out_cols] -- MXFP4 packed two per byte, element 2i in the low
  * nibble of byte i; MXFP8 one E4M3 byte each -- and scales row-major
- * [out_rows][out_cols / 32].  x and codes must be 16-byte aligned and
- * ld * element size a multiple of 16 bytes.  One kernel launch on `stream`;
- * nothing is allocated.  Returns NVFP4_ERR_INVALID_ARG, _SHAPE, _ALIGN,
- * _ARCH, _CUDA. */
+ * [out_rows][out_cols / 32], and, if scales_sw is not NULL, the same
+ * scale bytes in the MMA layout nvfp4_mx_gemm reads (offset
+ * ((r/128) * (padded scale cols / 4) + c/4) * 512 + (r%32)*16 + ((r/32)%4)*4
+ * + c%4 for row r, scale column c; padding written as zero).  x and codes
+ * must be 16-byte aligned and ld * element size a multiple of 16 bytes.  One
+ * kernel launch on `stream` (plus a memset of scales_sw when it has
+ * padding); nothing is allocated.  Returns NVFP4_ERR_INVALID_ARG, _SHAPE,
+ * _ALIGN, _ARCH, _CUDA. */
 nvfp4_status nvfp4_mx_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                                int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
-                               nvfp4_stream stream);
+                               void* scales_sw, nvfp4_stream stream);
+
+/* D bf16 [M, N] = A . B^T for MX operands, the comparison GEMMs (the page's
+ * quote of MXFP8 and MXFP4 block-scaled GEMMs on Blackwell):
+ *   D[m][n] = bf16_rn( sum_k deq(A)[m][k] * deq(B)[n][k] ),
+ *   deq = element value * 2^(scale byte - 127) over its 32-element block.
+ * A: a_codes [M][K] K-major as nvfp4_mx_quantize writes them (MXFP4: K/2
+ * bytes per row, MXFP8: K), a_scales_sw its scales in the MMA layout (the
+ * scales_sw output of nvfp4_mx_quantize); B likewise [N][K].  The WGRAD
+ * operands are the NVFP4_MX_COL outputs.  Shapes: K % 128 == 0, N % 8 == 0.
+ * All pointers device, 16-byte aligned.  One launch (the CTA-pair kernel,
+ * tcgen05 kind::mxf4nvf4 scale_vec::2X or kind::mxf8f6f4 scale_vec::1X).
+ * Returns NVFP4_ERR_INVALID_ARG, _SHAPE, _ALIGN, _ARCH, _CUDA. */
+nvfp4_status nvfp4_mx_gemm(const void* a_codes, const void* a_scales_sw, const void* b_codes,
+                           const void* b_scales_sw, int32_t fmt, void* D, int64_t M, int64_t N,
+                           int64_t K, nvfp4_stream stream);
 
 /* ---------------------------------------------------------------------- */
 /* Block-scaled GEMM                                                       */

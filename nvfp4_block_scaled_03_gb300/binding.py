@@ -72,8 +72,9 @@ def _load():
                        C.c_int),
         "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
                           C.c_int),
-        "nvfp4_mx_sizes": ([i64, i64, i32, i32, P(sz), P(sz)], C.c_int),
-        "nvfp4_mx_quantize": ([vp, i32, i64, i64, i64, i32, i32, vp, vp, vp], C.c_int),
+        "nvfp4_mx_sizes": ([i64, i64, i32, i32, P(sz), P(sz), P(sz)], C.c_int),
+        "nvfp4_mx_quantize": ([vp, i32, i64, i64, i64, i32, i32, vp, vp, vp, vp], C.c_int),
+        "nvfp4_mx_gemm": ([vp, vp, vp, vp, i32, vp, i64, i64, i64, vp], C.c_int),
         "nvfp4_mlp_sizes": ([i64, i64, i64, P(sz), P(sz)], C.c_int),
         "nvfp4_mlp_fwd": ([P(MlpParams), vp, vp, vp, sz, vp, sz, vp], C.c_int),
         "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
@@ -232,16 +233,21 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int, flags: int = 0, seed: int
 
 
 def mx_sizes(rows, cols, mode, fmt):
-    c, s = C.c_size_t(), C.c_size_t()
-    _check(lib.nvfp4_mx_sizes(rows, cols, mode, fmt, C.byref(c), C.byref(s)), "nvfp4_mx_sizes")
-    return c.value, s.value
+    """(codes, scales, scales in the MMA layout) byte sizes."""
+    c, s, w = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    _check(lib.nvfp4_mx_sizes(rows, cols, mode, fmt, C.byref(c), C.byref(s), C.byref(w)),
+           "nvfp4_mx_sizes")
+    return c.value, s.value, w.value
 
 
 def nvfp4_mx_quantize(x: torch.Tensor, mode: int, fmt: int, codes: torch.Tensor | None = None,
-                      scales: torch.Tensor | None = None, stream=None):
+                      scales: torch.Tensor | None = None, scales_sw: torch.Tensor | None = None,
+                      stream=None):
     """MXFP4 / MXFP8 quantisation of a 2-D bf16/fp32 CUDA tensor (see
     nvfp4_mx_quantize in nvfp4.h); returns (codes, scales) as uint8 tensors
-    shaped [out_rows, out_cols/2 or out_cols] and [out_rows, out_cols/32]."""
+    shaped [out_rows, out_cols/2 or out_cols] and [out_rows, out_cols/32].
+    ``scales_sw`` (optional, uint8, mx_sizes()[2] bytes) also receives the
+    scales in the MMA layout nvfp4_mx_gemm reads."""
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a 2-D tensor with unit column stride")
     dt = {torch.bfloat16: IN_BF16, torch.float32: IN_FP32}.get(x.dtype)
@@ -249,17 +255,31 @@ def nvfp4_mx_quantize(x: torch.Tensor, mode: int, fmt: int, codes: torch.Tensor 
         raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
     rows, cols = x.shape
     orows, ocols = (cols, rows) if mode == MX_COL else (rows, cols)
-    cb, sb = mx_sizes(rows, cols, mode, fmt)
+    cb, sb, swb = mx_sizes(rows, cols, mode, fmt)
     if codes is None:
         codes = torch.empty(orows, cb // orows, dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty(orows, sb // orows, dtype=torch.uint8, device=x.device)
-    if codes.numel() < cb or scales.numel() < sb:
+    if codes.numel() < cb or scales.numel() < sb or (scales_sw is not None and
+                                                     scales_sw.numel() < swb):
         raise ValueError("output buffers are smaller than nvfp4_mx_sizes gives")
     _check(lib.nvfp4_mx_quantize(x.data_ptr(), dt, rows, cols, x.stride(0), mode, fmt,
-                                 codes.data_ptr(), scales.data_ptr(), _stream(stream)),
+                                 codes.data_ptr(), scales.data_ptr(), _ptr(scales_sw),
+                                 _stream(stream)),
            "nvfp4_mx_quantize")
     return codes, scales
+
+
+def nvfp4_mx_gemm(a_codes: torch.Tensor, a_scales_sw: torch.Tensor, b_codes: torch.Tensor,
+                  b_scales_sw: torch.Tensor, fmt: int, M: int, N: int, K: int,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D bf16 [M, N] = A . B^T for MX operands (see nvfp4_mx_gemm in nvfp4.h)."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    _check(lib.nvfp4_mx_gemm(a_codes.data_ptr(), a_scales_sw.data_ptr(), b_codes.data_ptr(),
+                             b_scales_sw.data_ptr(), fmt, out.data_ptr(), M, N, K,
+                             _stream(stream)), "nvfp4_mx_gemm")
+    return out
 
 
 def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,

@@ -104,15 +104,22 @@ nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t c
 }
 
 nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
-                            size_t* codes_bytes, size_t* scales_bytes) {
-  return mx_sizes_impl(rows, cols, mode, fmt, codes_bytes, scales_bytes);
+                            size_t* codes_bytes, size_t* scales_bytes, size_t* scales_sw_bytes) {
+  return mx_sizes_impl(rows, cols, mode, fmt, codes_bytes, scales_bytes, scales_sw_bytes);
 }
 
 nvfp4_status nvfp4_mx_quantize(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                                int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
-                               nvfp4_stream stream) {
-  return mx_quantize_impl(x, in_dtype, rows, cols, ld, mode, fmt, codes, scales,
+                               void* scales_sw, nvfp4_stream stream) {
+  return mx_quantize_impl(x, in_dtype, rows, cols, ld, mode, fmt, codes, scales, scales_sw,
                           static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_mx_gemm(const void* a_codes, const void* a_scales_sw, const void* b_codes,
+                           const void* b_scales_sw, int32_t fmt, void* D, int64_t M, int64_t N,
+                           int64_t K, nvfp4_stream stream) {
+  return gemm_mx_impl(a_codes, a_scales_sw, b_codes, b_scales_sw, fmt, D, M, N, K,
+                      static_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,

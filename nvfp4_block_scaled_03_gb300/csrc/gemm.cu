@@ -36,7 +36,6 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps
 constexpr int kBM = 128;            // rows of A per tile (one MMA, cta_group::1)
 constexpr int kBKBytes = 128;       // K bytes per stage (256 FP4 elements)
-constexpr int kAtomsPerStage = 4;   // scale atoms per 128 rows per stage (K = 256)
 constexpr uint32_t kTmemCols = 512;
 
 struct GemmArgs {
@@ -399,12 +398,60 @@ constexpr int kPairBN = 256;
 constexpr int kPairCopyWarps = 2;
 constexpr int kThreadsPairCp = (2 + kPairCopyWarps + 8) * 32;  // producer, MMA, copy, epilogue
 
-template <int STAGES>
+// Operand formats of the pair kernel.  Every format stages 128 bytes of K per
+// row and issues four MMAs of 32 bytes of K per stage; the scale atoms (128
+// rows x 4 scale bytes, 512 bytes) cover 64 K elements for NVFP4 (one per
+// 16) and 128 for the MX formats (one per 32).
+enum { kFmtNVF4 = 0, kFmtMXF4 = 1, kFmtMXF8 = 2 };
+template <int FMT>
+struct PairFmt {
+  static constexpr int kAtoms = FMT == kFmtNVF4 ? 4 : (FMT == kFmtMXF4 ? 2 : 1);  // per stage
+  static constexpr int kStageK = FMT == kFmtMXF8 ? 128 : 256;  // K elements per stage
+  static constexpr int kMmaPerAtom = 4 / kAtoms;
+};
+
+// Instruction descriptor of the MX block-scaled MMAs: element format code for
+// A and B (E2M1 = 1 in the FP4 kinds, E4M3 = 0 in kind::mxf8f6f4), N / 8,
+// scale type UE8M0 (bit 23), M / 16; the scale factor IDs (bits 4-5 for B,
+// 29-30 for A: the first byte of each row's scale word the MMA reads) are
+// ORed in per MMA.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t fmt) {
+  return (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// The pair MMA of a format: NVFP4 (16-element blocks, UE4M3 scales), MXFP4
+// (32-element blocks: two UE8M0 scales per 64-deep MMA), MXFP8 (E4M3
+// elements, one UE8M0 scale per 32-deep MMA).
+template <int FMT>
+NVFP4_DEV void tc_mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (FMT == kFmtNVF4) {
+    tc_mma_pair_nvf4(d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem, accumulate);
+  } else if constexpr (FMT == kFmtMXF4) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+  }
+}
+
+template <int STAGES, int FMT = kFmtNVF4>
 struct PairSmem {
+  static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
-  static constexpr uint32_t kSFA = kAtomsPerStage * 512;       // own A rows' scale atoms
-  static constexpr uint32_t kSFB = 2 * kAtomsPerStage * 512;   // the tile's 256 B rows' scales
+  static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
+  static constexpr uint32_t kSFB = 2 * kAt * 512;              // the tile's 256 B rows' scales
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
@@ -420,7 +467,7 @@ struct PairSmem {
   static constexpr uint32_t kBytes = offStore + 8 * 2 * kStoreBox;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kSfCol0 = kPairBN;
-  static constexpr uint32_t kSfColsPerStage = 16 + 32;  // A (4 K steps x 4), B (4 x 8)
+  static constexpr uint32_t kSfColsPerStage = kAt * (4 + 8);  // A (4 per atom), B (8 per atom)
   static_assert(kSfCol0 + STAGES * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
   static_assert(kAlloc <= 232448, "shared memory overflow");
 };
@@ -442,14 +489,15 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
   }
 }
 
-template <int STAGES, int DMODE>
+template <int STAGES, int DMODE, int FMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
                           const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
-  using L = PairSmem<STAGES>;
+  using L = PairSmem<STAGES, FMT>;
+  constexpr int kAt = PairFmt<FMT>::kAtoms;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -468,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
   const bool leader = rank == 0;
   const uint32_t peer_abort = mapa_shared(smem_u32(smem + L::offMisc + 4), rank ^ 1u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_kb = (args.K + 255) / 256;
+  const int num_kb = (args.K + PairFmt<FMT>::kStageK - 1) / PairFmt<FMT>::kStageK;
   const int num_tiles = args.num_m_blk * args.num_n_blk;  // 256 x 256 tiles
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
@@ -517,13 +565,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
           tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
                            (b_rb0 + (int)rank) * 128);
-          // scale atoms as 128-byte rows: 4 atoms = 16 rows
+          // scale atoms as 128-byte rows (4 per atom)
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
-                           (a_rb * args.kg + kb * kAtomsPerStage) * 4);
+                           (a_rb * args.kg + kb * kAt) * 4);
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAtomsPerStage * 512), &tmSFB,
-                             fb, 0, ((b_rb0 + j) * args.kg + kb * kAtomsPerStage) * 4);
+            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAt * 512), &tmSFB, fb, 0,
+                             ((b_rb0 + j) * args.kg + kb * kAt) * 4);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -549,9 +597,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
             break;
           }
           tc_fence_after();
-          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const int natoms = min(kAt, args.kg - kb * kAt);
           const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sfb_t = sfa_t + 4 * kAt;
           const uint32_t sa = sbase + L::offSFA + s * L::kSFA;
           const uint32_t sb = sbase + L::offSFB + s * L::kSFB;
           for (int j = 0; j < natoms; ++j) {
@@ -559,9 +607,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
               tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb)
-              if ((4 + 2 * j + hb) % kPairCopyWarps == cw)
+              if ((kAt + 2 * j + hb) % kPairCopyWarps == cw)
                 tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4 * hb,
-                                          smem_desc_sf(sb + hb * (kAtomsPerStage * 512) + j * 512));
+                                          smem_desc_sf(sb + hb * (kAt * 512) + j * 512));
           }
           issued = true;
           tc_commit_pair(sf_bar(s), 1);  // the leader's barrier
@@ -576,7 +624,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA
-      constexpr uint32_t idesc = idesc_nvf4(256, kPairBN);
+      constexpr uint32_t idesc = FMT == kFmtNVF4 ? idesc_nvf4(256, kPairBN)
+                                 : idesc_mx(256, kPairBN, FMT == kFmtMXF8 ? 0u : 1u);
       uint32_t s = 0, ph = 0, acc_ph = 0;
       bool ok = true, issued = false;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
@@ -592,14 +641,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
             break;
           }
           tc_fence_after();
-          const int natoms = min(kAtomsPerStage, args.kg - kb * kAtomsPerStage);
+          const int nmma = min(kAt, args.kg - kb * kAt) * PairFmt<FMT>::kMmaPerAtom;
           const uint32_t sfa_t = tmem + L::kSfCol0 + s * L::kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + 16;
+          const uint32_t sfb_t = sfa_t + 4 * kAt;
           const uint32_t a0 = sbase + L::offA + s * L::kA;
           const uint32_t b0 = sbase + L::offB + s * L::kB;
-          for (int j = 0; j < natoms; ++j)
-            tc_mma_pair_nvf4(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
-                             idesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+          for (int j = 0; j < nmma; ++j) {
+            // MMA j reads 32 bytes of K per row; its scales are atom
+            // j / kMmaPerAtom, starting at byte (j % kMmaPerAtom) * kAt of
+            // each row's 4-byte scale word (the scale factor ID)
+            const int atom = j / PairFmt<FMT>::kMmaPerAtom;
+            const uint32_t sfid = (uint32_t)(j % PairFmt<FMT>::kMmaPerAtom) * kAt;
+            tc_mma_pair_bs<FMT>(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
+                                idesc | (sfid << 4) | (sfid << 29), sfa_t + 4 * atom,
+                                sfb_t + 8 * atom, (kb | j) != 0 ? 1u : 0u);
+          }
           issued = true;
           tc_commit_pair(empty_bar(s), 3);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -619,7 +675,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     const int ew = warp - 2 - kPairCopyWarps;  // epilogue warp 0..7
     const int q = warp & 3, h = ew >> 2;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
-    const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
+    const float alpha =
+        FMT == kFmtNVF4 ? __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b)) : 1.0f;
     uint8_t* stage_out = smem + L::offStore + ew * 2 * L::kStoreBox;
     if (DMODE == NVFP4_D_BF16 && lane == 0) prefetch_tmap(&tmD);
     uint32_t acc_ph = 0;
@@ -715,12 +772,12 @@ bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kby
 
 // 2-D map over a scale tensor viewed as rows of 128 bytes (4 rows per atom),
 // box of 16 rows (the 4 atoms of one stage).
-bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes) {
+bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes, int box_rows = 16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
   const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, 16};
+  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -742,12 +799,12 @@ bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int STAGES, int DMODE>
+template <int STAGES, int DMODE, int FMT = kFmtNVF4>
 nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
                          const CUtensorMap& msb, const CUtensorMap& md, const GemmArgs& a, int sms,
                          cudaStream_t stream) {
-  using L = PairSmem<STAGES>;
-  auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE>;
+  using L = PairSmem<STAGES, FMT>;
+  auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE, FMT>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
@@ -943,6 +1000,46 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   if (mc == 2) return launch_mode<256, 4, 2, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
   if (bn == 256) return launch_mode<256, 4, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
   return launch_mode<128, 6, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
+}
+
+// D bf16 [M, N] = A . B^T for MX operands (codes K-major; scales in the MMA
+// layout, one atom per 128 rows and 128 K elements), on the CTA-pair kernel.
+nvfp4_status gemm_mx_impl(const void* a_codes, const void* a_sf, const void* b_codes,
+                          const void* b_sf, int32_t fmt, void* D, int64_t M, int64_t N,
+                          int64_t K, cudaStream_t stream) {
+  if (!a_codes || !a_sf || !b_codes || !b_sf || !D) return NVFP4_ERR_INVALID_ARG;
+  if (fmt != NVFP4_MXFP4 && fmt != NVFP4_MXFP8) return NVFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 8) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(a_sf) || !aligned16(b_sf) ||
+      !aligned16(D))
+    return NVFP4_ERR_ALIGN;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  GemmArgs a = {};
+  a.sfa = static_cast<const uint8_t*>(a_sf);
+  a.sfb = static_cast<const uint8_t*>(b_sf);
+  a.D = D;
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.kg = (int)(K / 128);  // scale atoms per 128-row block along K
+  a.nrb_b = (int)((N + 127) / 128);
+  a.nrb_a = (int)((M + 127) / 128);
+  a.num_m_blk = (int)((M + 255) / 256);
+  a.num_n_blk = (int)((N + 255) / 256);
+  const int64_t kbytes = fmt == NVFP4_MXFP4 ? K / 2 : K;
+  const int atoms = fmt == NVFP4_MXFP4 ? PairFmt<kFmtMXF4>::kAtoms : PairFmt<kFmtMXF8>::kAtoms;
+  CUtensorMap ma, mb, msa, msb, md;
+  if (!make_code_map(&ma, a_codes, M, kbytes, 128) || !make_code_map(&mb, b_codes, N, kbytes, 128) ||
+      !make_sf_map(&msa, a_sf, (size_t)a.nrb_a * a.kg * 512, 4 * atoms) ||
+      !make_sf_map(&msb, b_sf, (size_t)a.nrb_b * a.kg * 512, 4 * atoms) ||
+      !make_out_map(&md, D, M, N))
+    return NVFP4_ERR_CUDA;
+  return fmt == NVFP4_MXFP4
+             ? launch_pair<5, NVFP4_D_BF16, kFmtMXF4>(ma, mb, msa, msb, md, a, dev.sm_count, stream)
+             : launch_pair<5, NVFP4_D_BF16, kFmtMXF8>(ma, mb, msa, msb, md, a, dev.sm_count, stream);
 }
 
 }  // namespace nvfp4

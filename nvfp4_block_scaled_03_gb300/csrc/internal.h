@@ -58,11 +58,15 @@ nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t co
 // Reads and clears the quantisers' device error word (after a sync).
 nvfp4_status quant_read_error(unsigned int* code);
 
+nvfp4_status gemm_mx_impl(const void* a_codes, const void* a_sf, const void* b_codes,
+                          const void* b_sf, int32_t fmt, void* D, int64_t M, int64_t N,
+                          int64_t K, cudaStream_t stream);
+
 nvfp4_status mx_sizes_impl(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
-                           size_t* codes_bytes, size_t* scales_bytes);
+                           size_t* codes_bytes, size_t* scales_bytes, size_t* scales_sw_bytes);
 nvfp4_status mx_quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                               int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
-                              cudaStream_t stream);
+                              void* scales_sw, cudaStream_t stream);
 
 inline nvfp4_status cuda_status(cudaError_t e) {
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;

@@ -68,7 +68,8 @@ template <typename T, int FMT>
 __global__ void __launch_bounds__(kMxThreads) mx_row_kernel(const T* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ld,
                                                             uint8_t* __restrict__ codes,
-                                                            uint8_t* __restrict__ scales) {
+                                                            uint8_t* __restrict__ scales,
+                                                            uint8_t* __restrict__ scales_sw) {
   const int64_t per_row = cols / 8, total = rows * per_row;
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -114,7 +115,10 @@ __global__ void __launch_bounds__(kMxThreads) mx_row_kernel(const T* __restrict_
       if (bad) w[0] = w[1] = 0;
       *reinterpret_cast<uint2*>(codes + r * cols + q * 8) = make_uint2(w[0], w[1]);
     }
-    if ((q & 3) == 0) scales[r * (cols / 32) + q / 4] = (uint8_t)sb;
+    if ((q & 3) == 0) {
+      scales[r * (cols / 32) + q / 4] = (uint8_t)sb;
+      if (scales_sw) scales_sw[sf_offset(r, q / 4, (cols / 32 + 3) / 4 * 4)] = (uint8_t)sb;
+    }
   }
 }
 
@@ -125,7 +129,8 @@ template <typename T, int FMT>
 __global__ void __launch_bounds__(kMxThreads) mx_col_kernel(const T* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ld,
                                                             uint8_t* __restrict__ codes,
-                                                            uint8_t* __restrict__ scales) {
+                                                            uint8_t* __restrict__ scales,
+                                                            uint8_t* __restrict__ scales_sw) {
   __shared__ float tile[32][kMxColTile + 1];
   const int64_t ctiles = (cols + kMxColTile - 1) / kMxColTile, rblocks = rows / 32;
   for (int64_t tix = blockIdx.x; tix < ctiles * rblocks; tix += gridDim.x) {
@@ -187,25 +192,27 @@ __global__ void __launch_bounds__(kMxThreads) mx_col_kernel(const T* __restrict_
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
       scales[c * (rows / 32) + rb] = (uint8_t)sb;
+      if (scales_sw) scales_sw[sf_offset(c, rb, (rows / 32 + 3) / 4 * 4)] = (uint8_t)sb;
     }
   }
 }
 
 template <typename T, int FMT>
 nvfp4_status launch_mx(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t mode,
-                       uint8_t* codes, uint8_t* scales, int sms, cudaStream_t stream) {
+                       uint8_t* codes, uint8_t* scales, uint8_t* scales_sw, int sms,
+                       cudaStream_t stream) {
   const T* xt = static_cast<const T*>(x);
   if (mode == NVFP4_MX_ROW) {
     const int64_t warps = (rows * (cols / 8) + 31) / 32;
     const int64_t grid = std::min<int64_t>((warps * 32 + kMxThreads - 1) / kMxThreads,
                                            (int64_t)sms * 16);
     mx_row_kernel<T, FMT><<<(unsigned)grid, kMxThreads, 0, stream>>>(xt, rows, cols, ld, codes,
-                                                                      scales);
+                                                                      scales, scales_sw);
   } else {
     const int64_t tiles = ((cols + kMxColTile - 1) / kMxColTile) * (rows / 32);
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)sms * 8);
     mx_col_kernel<T, FMT><<<(unsigned)grid, kMxThreads, 0, stream>>>(xt, rows, cols, ld, codes,
-                                                                      scales);
+                                                                      scales, scales_sw);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -213,7 +220,7 @@ nvfp4_status launch_mx(const void* x, int64_t rows, int64_t cols, int64_t ld, in
 }  // namespace
 
 nvfp4_status mx_sizes_impl(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
-                           size_t* codes_bytes, size_t* scales_bytes) {
+                           size_t* codes_bytes, size_t* scales_bytes, size_t* scales_sw_bytes) {
   if ((mode != NVFP4_MX_ROW && mode != NVFP4_MX_COL) || (fmt != NVFP4_MXFP4 && fmt != NVFP4_MXFP8))
     return NVFP4_ERR_INVALID_ARG;
   if (rows <= 0 || cols <= 0) return NVFP4_ERR_SHAPE;
@@ -222,15 +229,19 @@ nvfp4_status mx_sizes_impl(int64_t rows, int64_t cols, int32_t mode, int32_t fmt
   if (ocols % 32 || (mode == NVFP4_MX_COL && cols % 8)) return NVFP4_ERR_SHAPE;
   if (codes_bytes) *codes_bytes = (size_t)(orows * (fmt == NVFP4_MXFP4 ? ocols / 2 : ocols));
   if (scales_bytes) *scales_bytes = (size_t)(orows * (ocols / 32));
+  // the MMA layout: 512-byte atoms of 128 rows x 4 scale columns, padded
+  if (scales_sw_bytes)
+    *scales_sw_bytes = (size_t)(((orows + 127) / 128) * ((ocols / 32 + 3) / 4) * 512);
   return NVFP4_OK;
 }
 
 nvfp4_status mx_quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                               int64_t ld, int32_t mode, int32_t fmt, void* codes, void* scales,
-                              cudaStream_t stream) {
+                              void* scales_sw, cudaStream_t stream) {
   if (!x || !codes || !scales) return NVFP4_ERR_INVALID_ARG;
   if (in_dtype != NVFP4_IN_BF16 && in_dtype != NVFP4_IN_FP32) return NVFP4_ERR_INVALID_ARG;
-  nvfp4_status st = mx_sizes_impl(rows, cols, mode, fmt, nullptr, nullptr);
+  size_t sw_bytes = 0;
+  nvfp4_status st = mx_sizes_impl(rows, cols, mode, fmt, nullptr, nullptr, &sw_bytes);
   if (st != NVFP4_OK) return st;
   if (ld < cols || rows > INT32_MAX || cols > INT32_MAX) return NVFP4_ERR_SHAPE;
   const int64_t esize = in_dtype == NVFP4_IN_BF16 ? 2 : 4;
@@ -242,12 +253,21 @@ nvfp4_status mx_quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int
   if (st != NVFP4_OK) return st;
   uint8_t* c = static_cast<uint8_t*>(codes);
   uint8_t* s = static_cast<uint8_t*>(scales);
+  uint8_t* sw = static_cast<uint8_t*>(scales_sw);
+  const int64_t orows = mode == NVFP4_MX_COL ? cols : rows;
+  const int64_t ocols = mode == NVFP4_MX_COL ? rows : cols;
+  // padding entries of the MMA layout (rows to 128, scale columns to 4) read
+  // as zero
+  if (sw && (orows % 128 || (ocols / 32) % 4) &&
+      cudaMemsetAsync(sw, 0, sw_bytes, stream) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   const bool bf = in_dtype == NVFP4_IN_BF16;
+  const int n = dev.sm_count;
   if (fmt == NVFP4_MXFP4)
-    return bf ? launch_mx<uint16_t, NVFP4_MXFP4>(x, rows, cols, ld, mode, c, s, dev.sm_count, stream)
-              : launch_mx<float, NVFP4_MXFP4>(x, rows, cols, ld, mode, c, s, dev.sm_count, stream);
-  return bf ? launch_mx<uint16_t, NVFP4_MXFP8>(x, rows, cols, ld, mode, c, s, dev.sm_count, stream)
-            : launch_mx<float, NVFP4_MXFP8>(x, rows, cols, ld, mode, c, s, dev.sm_count, stream);
+    return bf ? launch_mx<uint16_t, NVFP4_MXFP4>(x, rows, cols, ld, mode, c, s, sw, n, stream)
+              : launch_mx<float, NVFP4_MXFP4>(x, rows, cols, ld, mode, c, s, sw, n, stream);
+  return bf ? launch_mx<uint16_t, NVFP4_MXFP8>(x, rows, cols, ld, mode, c, s, sw, n, stream)
+            : launch_mx<float, NVFP4_MXFP8>(x, rows, cols, ld, mode, c, s, sw, n, stream);
 }
 
 }  // namespace nvfp4
