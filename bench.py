@@ -38,7 +38,7 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # M=8192, N=14336, K=4096, from one ncu capture of that launch
 # (dram__bytes_read.sum 53.2 MB + dram__bytes_write.sum 188.1 MB); None once
 # the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = 53.143552e6 + 187.872512e6  # dram read + write, one FPROP launch
+FPROP_TRAFFIC_BYTES = None  # re-captured after each change of the GEMM kernel
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
@@ -737,22 +737,49 @@ def run_gemm_405b(args):
         calls = {"fprop": lambda: nv.nvfp4_gemm(qX, qW, out=out["fprop"]),
                  "dgrad": lambda: nv.nvfp4_gemm(qdY, qW, b_view=1, out=out["dgrad"]),
                  "wgrad": lambda: nv.nvfp4_gemm(qdYc, qXc, out=out["wgrad"])}
-        for g, fn in calls.items():
+        def record(fmt, g, fn):
             ms, ms_min = _timed(fn, reps, flush_l2)
             tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-            results.append({"projection": proj, "gemm": g, "M": M, "N": N, "K": K,
+            peak = fp4_peak if fmt != "mxfp8" else fp4_peak / 2
+            results.append({"format": fmt, "projection": proj, "gemm": g, "M": M, "N": N, "K": K,
                             "shape_MxNxK": {"fprop": [M, N, K], "dgrad": [M, K, N],
                                             "wgrad": [N, K, M]}[g],
                             "ms": round(ms, 4), "ms_min": round(ms_min, 4),
-                            "tflops": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4)})
-        del qX, qXc, qW, qdY, qdYc, out, calls
+                            "tflops": round(tf, 1), "frac_peak": round(tf / peak, 4)})
+        for g, fn in calls.items():
+            record("nvfp4", g, fn)
+        del qX, qXc, qW, qdY, qdYc, calls
+        torch.cuda.empty_cache()
+        # the same GEMMs with MX operands (32-element E8M0 blocks, RNE; DGRAD
+        # reads W quantised along N, WGRAD both operands along the tokens)
+        X = normal((M, K), seeds[0], 1.0, outliers=True)
+        W = normal((N, K), seeds[1], 0.02)
+        dY = normal((M, N), seeds[2], 1e-3)
+        for fmt, f in (("mxfp4", nv.MXFP4), ("mxfp8", nv.MXFP8)):
+            def mxq(t, mode):
+                rows, cols = t.shape
+                sw = torch.empty(nv.mx_sizes(rows, cols, mode, f)[2], dtype=torch.uint8,
+                                 device=device)
+                codes, _ = nv.nvfp4_mx_quantize(t, mode, f, scales_sw=sw)
+                return codes, sw
+            xr, wr, dyr = mxq(X, nv.MX_ROW), mxq(W, nv.MX_ROW), mxq(dY, nv.MX_ROW)
+            wc, dyc, xc = mxq(W, nv.MX_COL), mxq(dY, nv.MX_COL), mxq(X, nv.MX_COL)
+            mcalls = {"fprop": lambda: nv.nvfp4_mx_gemm(*xr, *wr, f, M, N, K, out=out["fprop"]),
+                      "dgrad": lambda: nv.nvfp4_mx_gemm(*dyr, *wc, f, M, K, N, out=out["dgrad"]),
+                      "wgrad": lambda: nv.nvfp4_mx_gemm(*dyc, *xc, f, N, K, M, out=out["wgrad"])}
+            for g, fn in mcalls.items():
+                record(fmt, g, fn)
+            del xr, wr, dyr, wc, dyc, xc, mcalls
+        del X, W, dY, out
         torch.cuda.empty_cache()
     clk = clocks.stop()
     nv.check_device_errors()
-    flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in results)
-    ms_all = sum(r["ms"] for r in results)
+    nvr = [r for r in results if r["format"] == "nvfp4"]
+    flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in nvr)
+    ms_all = sum(r["ms"] for r in nvr)
     print(json.dumps({
-        "metric": "NVFP4 GEMM TFLOP/s, Llama-3.1-405B MLP up and down projections (6 GEMMs)",
+        "metric": "NVFP4 GEMM TFLOP/s, Llama-3.1-405B MLP up and down projections (6 GEMMs; "
+                  "the same GEMMs in MXFP4 and MXFP8 listed for comparison)",
         "value": round(flops / (ms_all * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
         "higher_is_better": True, "n_gpus": 1, "dtype": "nvfp4",
         "data": "synthetic, seeded torch CUDA generators: X, H ~ N(0,1) with x50 outliers at "
@@ -761,6 +788,8 @@ def run_gemm_405b(args):
                                "[8192,53248]x[16384,53248]^T; FPROP, DGRAD, WGRAD each",
                    "reps": reps, "l2": "flushed before every timed GEMM (untimed)"},
         "peak_tflops": round(fp4_peak, 1),
+        "peak_note": "frac_peak: FP4 formats against the FP4 peak, MXFP8 against half of it "
+                     "(the nominal fp8/fp4 ratio)",
         "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)",
         "results": results, "clocks": clk, "impl": "ours"}), flush=True)
 

@@ -450,8 +450,12 @@ struct PairSmem {
   static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
+  // NVFP4: B's scales as four 4 KB images (one per K step: the two row
+  // halves' atoms, each repeated for the four 32-lane quarters) that one
+  // 128-lane x 256-bit copy each moves into tensor memory
+  static constexpr bool kImg = FMT == kFmtNVF4;
   static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
-  static constexpr uint32_t kSFB = 2 * kAt * 512;              // the tile's 256 B rows' scales
+  static constexpr uint32_t kSFB = kImg ? kAt * 4096 : 2 * kAt * 512;  // the tile's B scales
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
@@ -460,11 +464,11 @@ struct PairSmem {
   static constexpr uint32_t offBar = offSFB + STAGES * kSFB;
   static constexpr uint32_t kNumBars = 3 * STAGES + 3 + kPairCopyWarps;  // full, empty, scales-ready, acc x2, drains
   static constexpr uint32_t offMisc = offBar + kNumBars * 8;
-  // bf16 output staging for tensor stores: 2 boxes of 32 rows x 64 bytes per
+  // bf16 output staging for tensor stores: one box of 32 rows x 64 bytes per
   // epilogue warp
   static constexpr uint32_t kStoreBox = 32 * 64;
   static constexpr uint32_t offStore = (offMisc + 16 + 127) / 128 * 128;
-  static constexpr uint32_t kBytes = offStore + 8 * 2 * kStoreBox;
+  static constexpr uint32_t kBytes = offStore + 8 * kStoreBox;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kSfCol0 = kPairBN;
   static constexpr uint32_t kSfColsPerStage = kAt * (4 + 8);  // A (4 per atom), B (8 per atom)
@@ -568,10 +572,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           // scale atoms as 128-byte rows (4 per atom)
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
                            (a_rb * args.kg + kb * kAt) * 4);
+          if constexpr (L::kImg) {
+            tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAt * 512), &tmSFB, fb, 0,
-                             ((b_rb0 + j) * args.kg + kb * kAt) * 4);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAt * 512), &tmSFB, fb, 0,
+                               ((b_rb0 + j) * args.kg + kb * kAt) * 4);
+          }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -605,11 +613,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           for (int j = 0; j < natoms; ++j) {
             if (j % kPairCopyWarps == cw)
               tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
+            if constexpr (L::kImg) {
+              if ((kAt + j) % kPairCopyWarps == cw)
+                tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
+            } else {
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-              if ((kAt + 2 * j + hb) % kPairCopyWarps == cw)
-                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4 * hb,
-                                          smem_desc_sf(sb + hb * (kAt * 512) + j * 512));
+              for (int hb = 0; hb < 2; ++hb)
+                if ((kAt + 2 * j + hb) % kPairCopyWarps == cw)
+                  tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4 * hb,
+                                            smem_desc_sf(sb + hb * (kAt * 512) + j * 512));
+            }
           }
           issued = true;
           tc_commit_pair(sf_bar(s), 1);  // the leader's barrier
@@ -677,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
     const float alpha =
         FMT == kFmtNVF4 ? __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b)) : 1.0f;
-    uint8_t* stage_out = smem + L::offStore + ew * 2 * L::kStoreBox;
+    uint8_t* stage_out = smem + L::offStore + ew * L::kStoreBox;
     if (DMODE == NVFP4_D_BF16 && lane == 0) prefetch_tmap(&tmD);
     uint32_t acc_ph = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
@@ -698,12 +711,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
       if (DMODE == NVFP4_D_BF16) {
         // each 32-column chunk: bf16 rows into a staging box (lane = row; the
         // 16-byte pieces rotated so a warp's writes hit distinct banks), then
-        // one tensor store; the box is reused two stores later
+        // one tensor store; the box is rewritten once the store has read it
         const int32_t row0 = m_blk * 256 + (int)rank * 128 + q * 32;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
-          uint8_t* box = stage_out + (c & 1) * L::kStoreBox;
-          if (lane == 0) bulk_wait_group_read<1>();
+          uint8_t* box = stage_out;
+          if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
           uint32_t pk[16];
 #pragma unroll
@@ -780,6 +793,24 @@ bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes, int box_rows 
   const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 5-D map over a scale tensor (atoms of 4 rows x 128 bytes, kg per 128-row
+// block) that reads each atom four times: dimensions (byte, atom row, copy
+// [stride 0], row block, atom along K); a box of (128, 4, 4, 2, 4) brings one
+// stage's B scales (4 K steps x 2 row blocks) as 4 KB images, each two 2 KB
+// planes of one atom repeated for the four 32-lane quarters.
+bool make_sf_image_map(CUtensorMap* map, const void* base, int kg, int64_t row_blocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[5] = {128, 4, 4, (cuuint64_t)row_blocks, (cuuint64_t)kg};
+  const cuuint64_t strides[4] = {128, 0, (cuuint64_t)kg * 512, 512};
+  const cuuint32_t box[5] = {128, 4, 4, 2, 4};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -976,7 +1007,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     CUtensorMap msa, msb, md;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
         !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
-        !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
+        !make_sf_image_map(&msb, b_sf, a.kg, a.nrb_b))
       return NVFP4_ERR_CUDA;
     // bf16 output map for the tensor-store epilogue (other modes do not use it)
     if (d_mode == NVFP4_D_BF16) {
@@ -986,7 +1017,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     }
     a.num_m_blk = (int)((M + 255) / 256);
     a.num_n_blk = (int)((N + 255) / 256);
-    return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
+    return launch_pair_mode<4>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
   }
   const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
   const int mc = tile == NVFP4_TILE_128X256_MC2 ? 2 : 1;
