@@ -153,7 +153,6 @@ NVFP4_DEV int64_t sf_offset(int64_t r, int64_t c, int64_t pc4) {
   return ((r >> 7) * (pc4 >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
 }
 
-NVFP4_DEV float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 // ---------------------------------------------------------------------------
 // Shared memory / mbarrier / TMA
@@ -308,10 +307,6 @@ NVFP4_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-NVFP4_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
 }
 // Relaxed arrive on an mbarrier of any CTA in the cluster: no release fence,
 // so it does not wait for the thread's earlier memory operations (bulk tensor

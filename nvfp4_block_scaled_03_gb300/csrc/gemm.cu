@@ -88,20 +88,6 @@ NVFP4_DEV uint64_t smem_desc_kmajor(uint32_t saddr) {
   return d;
 }
 
-NVFP4_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                            unsigned int code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      *abort_flag = 1;
-      atomicCAS(&g_gemm_error, 0u, code);
-      return false;
-    }
-  }
-}
 
 // Drain wait used after an abort: bounded, ignores the abort flag.
 NVFP4_DEV void wait_drain(uint32_t bar, uint32_t parity) {
