@@ -436,12 +436,11 @@ struct PairSmem {
   static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
-  // NVFP4: B's scales as four 4 KB images (one per K step: the two row
-  // halves' atoms, each repeated for the four 32-lane quarters) that one
+  // B's scales as 4 KB images, one per scale atom along K (the two row
+  // halves' atoms, each repeated for the four 32-lane quarters), that one
   // 128-lane x 256-bit copy each moves into tensor memory
-  static constexpr bool kImg = FMT == kFmtNVF4;
   static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
-  static constexpr uint32_t kSFB = kImg ? kAt * 4096 : 2 * kAt * 512;  // the tile's B scales
+  static constexpr uint32_t kSFB = kAt * 4096;                 // the tile's B scale images
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
@@ -558,14 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           // scale atoms as 128-byte rows (4 per atom)
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
                            (a_rb * args.kg + kb * kAt) * 4);
-          if constexpr (L::kImg) {
-            tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + j * (kAt * 512), &tmSFB, fb, 0,
-                               ((b_rb0 + j) * args.kg + kb * kAt) * 4);
-          }
+          tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -578,9 +570,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
   } else if (warp >= 2 && warp < 2 + kPairCopyWarps) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- scale copies
-      // the stage's copies in the order A atom j (index j), B atom of K step j
-      // and row half hb (index 4 + 2 j + hb); copy warp cw issues the indices
-      // equal to cw modulo the number of copy warps
+      // the stage's copies: A's atom j (index j) and B's image of atom j (both
+      // row halves; index kAt + j); copy warp cw issues the indices equal to
+      // cw modulo the number of copy warps
       const int cw = warp - 2;
       uint32_t s = 0, ph = 0;
       bool ok = true, issued = false;
@@ -599,16 +591,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           for (int j = 0; j < natoms; ++j) {
             if (j % kPairCopyWarps == cw)
               tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
-            if constexpr (L::kImg) {
-              if ((kAt + j) % kPairCopyWarps == cw)
-                tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
-            } else {
-#pragma unroll
-              for (int hb = 0; hb < 2; ++hb)
-                if ((kAt + 2 * j + hb) % kPairCopyWarps == cw)
-                  tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4 * hb,
-                                            smem_desc_sf(sb + hb * (kAt * 512) + j * 512));
-            }
+            if ((kAt + j) % kPairCopyWarps == cw)
+              tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
           }
           issued = true;
           tc_commit_pair(sf_bar(s), 1);  // the leader's barrier
@@ -786,15 +770,16 @@ bool make_sf_map(CUtensorMap* map, const void* base, size_t bytes, int box_rows 
 
 // 5-D map over a scale tensor (atoms of 4 rows x 128 bytes, kg per 128-row
 // block) that reads each atom four times: dimensions (byte, atom row, copy
-// [stride 0], row block, atom along K); a box of (128, 4, 4, 2, 4) brings one
-// stage's B scales (4 K steps x 2 row blocks) as 4 KB images, each two 2 KB
-// planes of one atom repeated for the four 32-lane quarters.
-bool make_sf_image_map(CUtensorMap* map, const void* base, int kg, int64_t row_blocks) {
+// [stride 0], row block, atom along K); a box of (128, 4, 4, 2, atoms) brings
+// one stage's B scales (its atoms x 2 row blocks) as 4 KB images, each two
+// 2 KB planes of one atom repeated for the four 32-lane quarters.
+bool make_sf_image_map(CUtensorMap* map, const void* base, int kg, int64_t row_blocks,
+                       int atoms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[5] = {128, 4, 4, (cuuint64_t)row_blocks, (cuuint64_t)kg};
   const cuuint64_t strides[4] = {128, 0, (cuuint64_t)kg * 512, 512};
-  const cuuint32_t box[5] = {128, 4, 4, 2, 4};
+  const cuuint32_t box[5] = {128, 4, 4, 2, (cuuint32_t)atoms};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -993,7 +978,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     CUtensorMap msa, msb, md;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
         !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
-        !make_sf_image_map(&msb, b_sf, a.kg, a.nrb_b))
+        !make_sf_image_map(&msb, b_sf, a.kg, a.nrb_b, PairFmt<kFmtNVF4>::kAtoms))
       return NVFP4_ERR_CUDA;
     // bf16 output map for the tensor-store epilogue (other modes do not use it)
     if (d_mode == NVFP4_D_BF16) {
@@ -1051,7 +1036,7 @@ nvfp4_status gemm_mx_impl(const void* a_codes, const void* a_sf, const void* b_c
   CUtensorMap ma, mb, msa, msb, md;
   if (!make_code_map(&ma, a_codes, M, kbytes, 128) || !make_code_map(&mb, b_codes, N, kbytes, 128) ||
       !make_sf_map(&msa, a_sf, (size_t)a.nrb_a * a.kg * 512, 4 * atoms) ||
-      !make_sf_map(&msb, b_sf, (size_t)a.nrb_b * a.kg * 512, 4 * atoms) ||
+      !make_sf_image_map(&msb, b_sf, a.kg, a.nrb_b, atoms) ||
       !make_out_map(&md, D, M, N))
     return NVFP4_ERR_CUDA;
   return fmt == NVFP4_MXFP4
