@@ -38,7 +38,7 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # M=8192, N=14336, K=4096, from one ncu capture of that launch
 # (dram__bytes_read.sum 53.2 MB + dram__bytes_write.sum 188.1 MB); None once
 # the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = 52.609280e6 + 188.834816e6  # dram read + write, one FPROP launch
+FPROP_TRAFFIC_BYTES = 52.615424e6 + 188.206080e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
