@@ -317,6 +317,38 @@ typedef struct nvfp4_mlp_params {
   uint32_t flags;  /* NVFP4_RHT or 0                                 */
 } nvfp4_mlp_params;
 
+/* SwiGLU between the gate/up and down projections, with the tensor amaxes of
+ * its outputs for the NVFP4 quantisations that follow ("NVFP4 pretraining
+ * recipe" page, Figure 1 text and bullets 3-5: each output is quantised
+ * row-wise for FPROP / DGRAD and column-wise, with the RHT when enabled, for
+ * WGRAD; both need its per-tensor amax).  Computed in FP32 with the CUDA
+ * expf, each output rounded once to bf16:
+ *   forward   H  = silu(G) * U,               silu(g) = g sigmoid(g)
+ *   backward  dU = dH * silu(G),  dG = dH * U * sigmoid(G) (1 + G (1 - sigmoid(G)))
+ * All tensors bf16 [rows, cols], contiguous, 16-byte aligned; rows % 16 == 0,
+ * cols % 8 == 0.  For each output T the kernel writes two device floats,
+ * taken from the bf16 values it stores (no second read of T):
+ *   amax_*_row = max |T|, the amax of T's ROW_1X16 quantisation;
+ *   amax_*_col = with NVFP4_RHT in flags, max |(1/4) H16 diag(s) v| over every
+ *                16-row block v of every column of T, signs s from `seed`
+ *                as in nvfp4_quantize; otherwise max |T| again.
+ * Each equals, bit for bit, what nvfp4_amax returns for T, so it can be given
+ * to nvfp4_quantize with NVFP4_AMAX_GIVEN.  workspace: device scratch of at
+ * least nvfp4_swiglu_workspace_bytes(), 16-byte aligned, contents on return
+ * unspecified.  Two kernel launches on `stream`; nothing is allocated.
+ * Returns NVFP4_ERR_INVALID_ARG (a NULL pointer, unknown flag bits),
+ * _SHAPE, _ALIGN, _WORKSPACE, _ARCH, _CUDA. */
+size_t nvfp4_swiglu_workspace_bytes(void);
+nvfp4_status nvfp4_swiglu_fwd(const void* G, const void* U, void* H, int64_t rows, int64_t cols,
+                              uint32_t flags, uint64_t seed, float* amax_h_row,
+                              float* amax_h_col, void* workspace, size_t workspace_bytes,
+                              nvfp4_stream stream);
+nvfp4_status nvfp4_swiglu_bwd(const void* dH, const void* G, const void* U, void* dG, void* dU,
+                              int64_t rows, int64_t cols, uint32_t flags, uint64_t seed,
+                              float* amax_dg_row, float* amax_dg_col, float* amax_du_row,
+                              float* amax_du_col, void* workspace, size_t workspace_bytes,
+                              nvfp4_stream stream);
+
 /* Device bytes of the saved-activation buffer (forward -> backward) and of
  * the workspace either call needs. */
 nvfp4_status nvfp4_mlp_sizes(int64_t M, int64_t D, int64_t F, size_t* saved_bytes,

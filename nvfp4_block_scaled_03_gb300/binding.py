@@ -75,6 +75,10 @@ def _load():
         "nvfp4_mx_sizes": ([i64, i64, i32, i32, P(sz), P(sz), P(sz)], C.c_int),
         "nvfp4_mx_quantize": ([vp, i32, i64, i64, i64, i32, i32, vp, vp, vp, vp], C.c_int),
         "nvfp4_mx_gemm": ([vp, vp, vp, vp, i32, vp, i64, i64, i64, vp], C.c_int),
+        "nvfp4_swiglu_workspace_bytes": ([], sz),
+        "nvfp4_swiglu_fwd": ([vp, vp, vp, i64, i64, u32, u64, vp, vp, vp, sz, vp], C.c_int),
+        "nvfp4_swiglu_bwd": ([vp, vp, vp, vp, vp, i64, i64, u32, u64, vp, vp, vp, vp, vp, sz, vp],
+                             C.c_int),
         "nvfp4_mlp_sizes": ([i64, i64, i64, P(sz), P(sz)], C.c_int),
         "nvfp4_mlp_fwd": ([P(MlpParams), vp, vp, vp, sz, vp, sz, vp], C.c_int),
         "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
@@ -207,8 +211,8 @@ def nvfp4_amax(x: torch.Tensor, amax_plain: torch.Tensor | None = None,
         if t is not None and (t.dtype != torch.float32 or t.numel() != 1 or not t.is_cuda):
             raise ValueError("amax outputs must be 1-element float32 CUDA tensors")
     rows, cols = x.shape
-    if workspace is None:
-        workspace = _workspace(quantize_sizes(rows, cols, ROW_1X16)[3], x.device)
+    if workspace is None:  # the partial-maxima workspace does not depend on the shape
+        workspace = _workspace(quantize_sizes(128, 128, ROW_1X16)[3], x.device)
     _check(lib.nvfp4_amax(x.data_ptr(), dt, rows, cols, x.stride(0), seed, _ptr(amax_plain),
                           _ptr(amax_rht), _ptr(workspace), workspace.numel(), _stream(stream)),
            "nvfp4_amax")
@@ -301,6 +305,52 @@ def nvfp4_gemm(A: QTensor, B: QTensor, a_view: int = 0, b_view: int = 0,
                             d_mode, _ptr(C_add), M, N, K, None, 0, _stream(stream))
     _check(st, "nvfp4_gemm")
     return out
+
+
+def _bf16_2d(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("SwiGLU tensors must be contiguous 2-D bf16 CUDA tensors")
+        if t.shape != ts[0].shape:
+            raise ValueError("SwiGLU tensors must have one shape")
+
+
+def _amax_outs(n, device):
+    return [torch.zeros(1, dtype=torch.float32, device=device) for _ in range(n)]
+
+
+def nvfp4_swiglu_fwd(G, U, rht=True, seed=0, H=None, workspace=None, stream=None):
+    """H = silu(G) * U with the amaxes of H's row-wise and column-wise (RHT)
+    quantisations (see nvfp4_swiglu_fwd in nvfp4.h); returns
+    (H, amax_row, amax_col), the amaxes as 1-element float32 CUDA tensors."""
+    H = torch.empty_like(G) if H is None else H
+    _bf16_2d(G, U, H)
+    rows, cols = G.shape
+    if workspace is None:
+        workspace = _workspace(lib.nvfp4_swiglu_workspace_bytes(), G.device)
+    a_row, a_col = _amax_outs(2, G.device)
+    _check(lib.nvfp4_swiglu_fwd(G.data_ptr(), U.data_ptr(), H.data_ptr(), rows, cols,
+                                RHT if rht else 0, seed, a_row.data_ptr(), a_col.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "nvfp4_swiglu_fwd")
+    return H, a_row, a_col
+
+
+def nvfp4_swiglu_bwd(dH, G, U, rht=True, seed=0, workspace=None, stream=None):
+    """dG, dU of the SwiGLU with the amaxes of their row-wise and column-wise
+    quantisations; returns (dG, dU, amax_dg_row, amax_dg_col, amax_du_row,
+    amax_du_col)."""
+    dG, dU = torch.empty_like(G), torch.empty_like(G)
+    _bf16_2d(dH, G, U, dG, dU)
+    rows, cols = G.shape
+    if workspace is None:
+        workspace = _workspace(lib.nvfp4_swiglu_workspace_bytes(), G.device)
+    a = _amax_outs(4, G.device)
+    _check(lib.nvfp4_swiglu_bwd(dH.data_ptr(), G.data_ptr(), U.data_ptr(), dG.data_ptr(),
+                                dU.data_ptr(), rows, cols, RHT if rht else 0, seed,
+                                *(t.data_ptr() for t in a), workspace.data_ptr(),
+                                workspace.numel(), _stream(stream)), "nvfp4_swiglu_bwd")
+    return (dG, dU, *a)
 
 
 def mlp_sizes(M, D, F):

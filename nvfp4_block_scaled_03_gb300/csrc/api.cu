@@ -103,6 +103,28 @@ nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t c
                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+size_t nvfp4_swiglu_workspace_bytes(void) { return kSwigluPartialsBytes; }
+
+nvfp4_status nvfp4_swiglu_fwd(const void* G, const void* U, void* H, int64_t rows, int64_t cols,
+                              uint32_t flags, uint64_t seed, float* amax_h_row,
+                              float* amax_h_col, void* workspace, size_t workspace_bytes,
+                              nvfp4_stream stream) {
+  if (flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  return swiglu_fwd_impl(G, U, H, rows, cols, seed, flags & NVFP4_RHT, amax_h_row, amax_h_col,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_swiglu_bwd(const void* dH, const void* G, const void* U, void* dG, void* dU,
+                              int64_t rows, int64_t cols, uint32_t flags, uint64_t seed,
+                              float* amax_dg_row, float* amax_dg_col, float* amax_du_row,
+                              float* amax_du_col, void* workspace, size_t workspace_bytes,
+                              nvfp4_stream stream) {
+  if (flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  return swiglu_bwd_impl(dH, G, U, dG, dU, rows, cols, seed, flags & NVFP4_RHT, amax_dg_row,
+                         amax_dg_col, amax_du_row, amax_du_col, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
 nvfp4_status nvfp4_mx_sizes(int64_t rows, int64_t cols, int32_t mode, int32_t fmt,
                             size_t* codes_bytes, size_t* scales_bytes, size_t* scales_sw_bytes) {
   return mx_sizes_impl(rows, cols, mode, fmt, codes_bytes, scales_bytes, scales_sw_bytes);

@@ -38,10 +38,21 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
 // Reads and clears the GEMM kernels' device error word (after a sync).
 nvfp4_status gemm_read_error(unsigned int* code);
 
-nvfp4_status swiglu_fwd_impl(const void* G, const void* U, void* H, int64_t n,
-                             cudaStream_t stream);
+// SwiGLU forward / backward on bf16 [rows, cols] tensors (rows % 16 == 0,
+// cols % 8 == 0), also writing the tensor amaxes of each bf16 output for its
+// row-wise (amax_*_row: max |x|) and column-wise (amax_*_col: max |RHT(x)|
+// over 16-row column blocks with the seed's signs when rht, else max |x|)
+// NVFP4 quantisations.  partials: 16-byte aligned device scratch of at least
+// kSwigluPartialsBytes.
+constexpr size_t kSwigluPartialsBytes = 4 * kMaxPartials * sizeof(float);
+nvfp4_status swiglu_fwd_impl(const void* G, const void* U, void* H, int64_t rows, int64_t cols,
+                             uint64_t seed, bool rht, float* amax_row, float* amax_col,
+                             void* partials, size_t partials_bytes, cudaStream_t stream);
 nvfp4_status swiglu_bwd_impl(const void* dH, const void* G, const void* U, void* dG, void* dU,
-                             int64_t n, cudaStream_t stream);
+                             int64_t rows, int64_t cols, uint64_t seed, bool rht,
+                             float* amax_dg_row, float* amax_dg_col, float* amax_du_row,
+                             float* amax_du_col, void* partials, size_t partials_bytes,
+                             cudaStream_t stream);
 
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry-point
 // query (null if the driver does not provide it).

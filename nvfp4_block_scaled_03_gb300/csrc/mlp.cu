@@ -50,6 +50,7 @@ struct Saved {
 };
 struct Work {
   void* partials;
+  void* sw_partials;  // the SwiGLU kernels' amax partial maxima
   nvfp4_tensor qX, qH, qdY, qdYc, qdG, qdGc, qdU, qdUc;
   void* H;
   void* dH;
@@ -73,6 +74,7 @@ void carve_saved(void* base, int64_t M, int64_t D, int64_t F, Saved* s, size_t* 
 void carve_work(void* base, int64_t M, int64_t D, int64_t F, Work* w, size_t* bytes) {
   Carver c(base);
   w->partials = c.take(kQuantWorkspaceBytes);
+  w->sw_partials = c.take(kSwigluPartialsBytes);
   carve_q(c, &w->qX, M, D, NVFP4_ROW_1X16, false);
   carve_q(c, &w->qH, M, F, NVFP4_ROW_1X16, false);
   carve_q(c, &w->qdY, M, D, NVFP4_ROW_1X16, false);
@@ -100,19 +102,23 @@ bool dims_ok(int64_t M, int64_t D, int64_t F) {
   } while (0)
 
 // A bf16 operand [rows, cols] quantised twice -- row-wise (FPROP / DGRAD
-// operand) and column-wise (WGRAD operand) -- with both tensor amaxes taken
-// from one read of x; the two quantise passes then use them as given.
+// operand) and column-wise (WGRAD operand).  With amax_given, row->amax and
+// col->amax already hold the tensor amaxes (written by the kernel that
+// produced x); otherwise both are taken from one read of x first.  The two
+// quantise passes then use them as given.
 nvfp4_status quantize_pair(const void* x, int64_t rows, int64_t cols, uint32_t row_flags,
                            uint32_t col_flags, uint64_t seed, uint64_t row_offset,
-                           uint64_t col_offset, nvfp4_tensor* row, nvfp4_tensor* col, void* ws,
-                           size_t wsb, cudaStream_t st) {
-  const bool rht = col_flags & NVFP4_RHT;
-  NVFP4_TRY(amax_impl(x, NVFP4_IN_BF16, rows, cols, cols, seed, row->amax,
-                      rht ? col->amax : nullptr, ws, wsb, st));
-  if (!rht &&
-      cudaMemcpyAsync(col->amax, row->amax, sizeof(float), cudaMemcpyDeviceToDevice, st) !=
-          cudaSuccess)
-    return NVFP4_ERR_CUDA;
+                           uint64_t col_offset, nvfp4_tensor* row, nvfp4_tensor* col,
+                           bool amax_given, void* ws, size_t wsb, cudaStream_t st) {
+  if (!amax_given) {
+    const bool rht = col_flags & NVFP4_RHT;
+    NVFP4_TRY(amax_impl(x, NVFP4_IN_BF16, rows, cols, cols, seed, row->amax,
+                        rht ? col->amax : nullptr, ws, wsb, st));
+    if (!rht &&
+        cudaMemcpyAsync(col->amax, row->amax, sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
   NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_ROW_1X16,
                           row_flags | NVFP4_AMAX_GIVEN, seed, row_offset, row, nullptr, 0, st));
   NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_COL_1X16,
@@ -165,11 +171,12 @@ nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, vo
                           &s.qWu, ws, wsb, st));
   NVFP4_TRY(quantize_impl(p->Wd, NVFP4_IN_FP32, D, F, F, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
                           &s.qWd, ws, wsb, st));
-  NVFP4_TRY(quantize_pair(X, M, D, 0, rht, p->seed, 0, 0, &w.qX, &s.qXc, ws, wsb, st));
+  NVFP4_TRY(quantize_pair(X, M, D, 0, rht, p->seed, 0, 0, &w.qX, &s.qXc, false, ws, wsb, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWg, 0, s.G, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWu, 0, s.U, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
-  NVFP4_TRY(swiglu_fwd_impl(s.G, s.U, w.H, M * F, st));
-  NVFP4_TRY(quantize_pair(w.H, M, F, 0, rht, p->seed, 0, 0, &w.qH, &s.qHc, ws, wsb, st));
+  NVFP4_TRY(swiglu_fwd_impl(s.G, s.U, w.H, M, F, p->seed, rht, w.qH.amax, s.qHc.amax,
+                            w.sw_partials, kSwigluPartialsBytes, st));
+  NVFP4_TRY(quantize_pair(w.H, M, F, 0, rht, p->seed, 0, 0, &w.qH, &s.qHc, true, ws, wsb, st));
   NVFP4_TRY(gemm_impl(&w.qH, 0, &s.qWd, 0, Y, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
   return NVFP4_OK;
 }
@@ -201,16 +208,18 @@ nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void
   const size_t wsb = kQuantWorkspaceBytes;
 
   NVFP4_TRY(quantize_pair(dY, M, D, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 0, o + 1, &w.qdY,
-                          &w.qdYc, ws, wsb, st));
+                          &w.qdYc, false, ws, wsb, st));
   // DGRAD of the down projection: dH = dY . Wd  (Wd read through its transpose)
   NVFP4_TRY(gemm_impl(&w.qdY, 0, &s.qWd, 1, w.dH, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   // WGRAD of the down projection: dWd += dY^T . H
   NVFP4_TRY(gemm_impl(&w.qdYc, 0, &s.qHc, 0, dWd, NVFP4_D_F32_ACCUM, nullptr, D, F, M, 0, st));
-  NVFP4_TRY(swiglu_bwd_impl(w.dH, s.G, s.U, w.dG, w.dU, M * F, st));
+  NVFP4_TRY(swiglu_bwd_impl(w.dH, s.G, s.U, w.dG, w.dU, M, F, p->seed, rht, w.qdG.amax,
+                            w.qdGc.amax, w.qdU.amax, w.qdUc.amax, w.sw_partials,
+                            kSwigluPartialsBytes, st));
   NVFP4_TRY(quantize_pair(w.dG, M, F, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 2, o + 3, &w.qdG,
-                          &w.qdGc, ws, wsb, st));
+                          &w.qdGc, true, ws, wsb, st));
   NVFP4_TRY(quantize_pair(w.dU, M, F, NVFP4_SR, rht | NVFP4_SR, p->seed, o + 4, o + 5, &w.qdU,
-                          &w.qdUc, ws, wsb, st));
+                          &w.qdUc, true, ws, wsb, st));
   // DGRAD of gate and up: dX = dG . Wg + dU . Wu (second GEMM adds the first)
   NVFP4_TRY(gemm_impl(&w.qdG, 0, &s.qWg, 1, w.dXg, NVFP4_D_BF16, nullptr, M, D, F, 0, st));
   NVFP4_TRY(gemm_impl(&w.qdU, 0, &s.qWu, 1, dX, NVFP4_D_BF16_ADD_C, w.dXg, M, D, F, 0, st));

@@ -170,29 +170,6 @@ NVFP4_DEV void load8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// ---- block-wide reductions ---------------------------------------------------
-NVFP4_DEV float warp_max(float m) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  return m;
-}
-
-// Max over all threads of the CTA (every thread gets the result).
-NVFP4_DEV float block_max(float m, float* red) {
-  m = warp_max(m);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (warp == 0) {
-    float t = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
-    t = warp_max(t);
-    if (lane == 0) red[0] = t;
-  }
-  __syncthreads();
-  return red[0];
-}
-
 // Per-tensor encode scale at the start of a quantise pass: reduce the amax
 // pass's partial maxima (or read the caller's amax); CTA 0 publishes amax and
 // s_dec.
@@ -213,34 +190,7 @@ NVFP4_DEV float tensor_s_enc(const QParams& p, float* red) {
   return s_enc;
 }
 
-// ---- random Hadamard transform -----------------------------------------------
-// Butterfly stages h < width inside one thread's contiguous elements.
-template <int N>
-NVFP4_DEV void butterfly_local(float (&v)[N]) {
-#pragma unroll
-  for (int h = 1; h < N; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
-      }
-    }
-  }
-}
-
-// Full 16-point transform of one register-resident block: signs, stages
-// h = 1, 2, 4, 8, then x 1/4.
-NVFP4_DEV void rht16_block(float (&v)[16], uint32_t sign_bits) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if ((sign_bits >> i) & 1u) v[i] = -v[i];
-  butterfly_local<16>(v);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
-}
-
+// ---- random Hadamard transform of a block split over a lane pair --------------
 // Transform of a block split over a lane pair (lane^1): this thread holds
 // elements half*8 .. half*8+7.  Stages h = 1, 2, 4 are local; h = 8 pairs
 // element i of the two halves through one shuffle.
