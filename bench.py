@@ -254,6 +254,28 @@ class Layer:
                 events[i][1].record()
 
 
+def host_link_gbs(host, dev, reps=3):
+    """Pinned host <-> device copy bandwidth of this machine (GB/s each way, best
+    of `reps`), measured just before the end-to-end loop: the copies of that
+    loop cannot run faster, and the link differs from one machine to the
+    next."""
+    import torch
+    n = min(host.numel(), dev.numel())
+    h, d = host.view(-1)[:n], dev.view(-1)[:n]
+    nbytes = n * host.element_size()
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        out[name] = round(nbytes / best / 1e9, 1)
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank = dist_init("nccl")
@@ -313,6 +335,7 @@ def run_ours(args):
     # ---- end to end through host buffers (H2D inputs, D2H outputs) ----------
     h2d = sum(t.numel() * t.element_size() for t in layer.host.values())
     d2h = sum(t.numel() * t.element_size() for t in layer.out_host.values())
+    link = host_link_gbs(layer.host["dY"], layer.sets[0]["dY"])
     # Pipelined like a training loop: step i's inputs go host -> device on one
     # copy stream and step i-1's outputs device -> host on another while the
     # compute stream runs; two sets of device buffers, ordered by events.
@@ -389,7 +412,9 @@ def run_ours(args):
                              "time including the amax pre-pass"},
         "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "host_link_gbs": link,
+                "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3)},
         "gpu_launches": layer.launches_per_step * args.steps,
         "clocks": clk,
     }
