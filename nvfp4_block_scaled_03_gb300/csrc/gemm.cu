@@ -153,22 +153,40 @@ NVFP4_DEV void store_row_chunk(const GemmArgs& a, int64_t row, int64_t col0, con
       *reinterpret_cast<uint4*>(D + g * 8) = o;
     }
   } else {  // NVFP4_D_F32_ACCUM: D += float(bf16(alpha * acc))
+    // the loads of four 16-byte pieces before their stores: the stores may
+    // alias later loads as far as the compiler knows, so interleaving them
+    // one by one would serialise eight memory round trips per chunk
     float* D = static_cast<float*>(a.D) + row * a.N + col0;
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      if (col0 + g * 4 >= a.N) break;
-      float4 d = *reinterpret_cast<const float4*>(D + g * 4);
-      float t[4];
+    for (int g0 = 0; g0 < 8; g0 += 4) {
+      float4 d[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        t[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__uint_as_float(r[g * 4 + e]), alpha)));
-      d.x = __fadd_rn(d.x, t[0]);
-      d.y = __fadd_rn(d.y, t[1]);
-      d.z = __fadd_rn(d.z, t[2]);
-      d.w = __fadd_rn(d.w, t[3]);
-      *reinterpret_cast<float4*>(D + g * 4) = d;
+      for (int g = 0; g < 4; ++g)
+        if (col0 + (g0 + g) * 4 < a.N) d[g] = *reinterpret_cast<const float4*>(D + (g0 + g) * 4);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (col0 + (g0 + g) * 4 >= a.N) break;
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          t[e] = __bfloat162float(
+              __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[(g0 + g) * 4 + e]), alpha)));
+        d[g].x = __fadd_rn(d[g].x, t[0]);
+        d[g].y = __fadd_rn(d[g].y, t[1]);
+        d[g].z = __fadd_rn(d[g].z, t[2]);
+        d[g].w = __fadd_rn(d[g].w, t[3]);
+        *reinterpret_cast<float4*>(D + (g0 + g) * 4) = d[g];
+      }
     }
   }
+}
+
+// Pulls the part of D that a row of a later tile's epilogue reads (128-byte
+// lines from col0 on, `bytes` of them) into L2 while the tile's MMAs run.
+NVFP4_DEV void prefetch_l2_row(const void* p, int bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int o = 0; o < bytes; o += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(c + o)));
 }
 
 template <int BN, int STAGES, int DMODE, int MC, int BKB>
@@ -665,6 +683,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     uint32_t acc_ph = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
       const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+      if (DMODE != NVFP4_D_BF16) {
+        // the rows of D (F32_ACCUM) or C (BF16_ADD_C) this warp reads for the
+        // tile: into L2 while the MMAs still run
+        const int64_t row = (int64_t)m_blk * 256 + rank * 128 + q * 32 + lane;
+        const int64_t col0 = (int64_t)n_blk * kPairBN + h * kCols;
+        if (row < args.M && col0 < args.N) {
+          const int esz = DMODE == NVFP4_D_F32_ACCUM ? 4 : 2;
+          const void* base = DMODE == NVFP4_D_F32_ACCUM ? args.D : args.C;
+          const int64_t ncol = args.N - col0 < kCols ? args.N - col0 : kCols;
+          prefetch_l2_row(static_cast<const char*>(base) + (row * args.N + col0) * esz,
+                          (int)(ncol * esz));
+        }
+      }
       if (!wait_bounded_pair(acc_full, acc_ph, abort_flag, peer_abort, 0x33u)) break;
       tc_fence_after();
       uint32_t r[kChunks][32];

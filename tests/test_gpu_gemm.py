@@ -90,6 +90,28 @@ def test_gemm_output_modes(nv, orc):
     nv.check_device_errors()
 
 
+@pytest.mark.parametrize("M,K,N", [(512, 256, 784), (768, 512, 512)])
+def test_gemm_output_modes_pair_kernel(nv, orc, M, K, N):
+    """The fold into FP32 and the bf16 add on the CTA-pair kernel (the large-
+    shape path), with a ragged last tile: F32_ACCUM equals W0 + float(D)
+    exactly, D the bf16 output of the same kernel; ADD_C is within the GEMM
+    tolerance of the FP64 product plus C."""
+    import torch
+    L = _layer(orc, M, K, N)
+    a, b = L["X"], L["W"]
+    A, B = H.upload(nv, a), H.upload(nv, b)
+    D = nv.nvfp4_gemm(A, B, tile=nv.TILE_PAIR_256X256)
+    rng = np.random.Generator(np.random.PCG64(5))
+    W0 = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).cuda()
+    acc = W0.clone()
+    nv.nvfp4_gemm(A, B, out=acc, d_mode=nv.D_F32_ACCUM, tile=nv.TILE_PAIR_256X256)
+    assert torch.equal(acc, W0 + D.float())
+    Cb = H.dev_bf16(syn.gradients((M, N), seed=9))
+    E = nv.nvfp4_gemm(A, B, d_mode=nv.D_BF16_ADD_C, C_add=Cb, tile=nv.TILE_PAIR_256X256)
+    H.assert_gemm_close(H.host_f64(E), orc.gemm_fp64(a, b) + H.host_f64(Cb), "ADD_C pair")
+    nv.check_device_errors()
+
+
 def test_gemm_end_to_end_gpu_quantiser(nv, orc):
     """GPU quantiser -> GPU GEMM for FPROP/DGRAD/WGRAD vs the oracle chain."""
     M, K, N = 256, 512, 768
