@@ -113,6 +113,34 @@ NVFP4_DEV void butterfly_local(float (&v)[N]) {
   }
 }
 
+// max |(H16 diag(s) v)_i| over one block, without the transform's x 1/4
+// (applied by the caller to its final maximum: rounding is monotone, so that
+// maximum is the same bit for bit).  Signs and butterfly stages h = 1, 2, 4
+// as in the full transform; the last stage turns each pair (a, b) into a + b
+// and a - b, and the larger magnitude of the two rounded results is exactly
+// the rounded |a| + |b| (one of them is that sum, the other is no larger),
+// so the stage is one add per pair.  v is overwritten.
+NVFP4_DEV float rht16_absmax_unscaled(float (&v)[16], uint32_t sign_bits) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((sign_bits >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, __fadd_rn(fabsf(v[i]), fabsf(v[i + 8])));
+  return m;
+}
+
 // Full 16-point transform of one register-resident block: signs, stages
 // h = 1, 2, 4, 8, then x 1/4.
 NVFP4_DEV void rht16_block(float (&v)[16], uint32_t sign_bits) {

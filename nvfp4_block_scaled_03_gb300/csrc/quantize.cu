@@ -708,10 +708,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
           b[e] = __uint_as_float(w & 0xFFFF0000u);
           if (PLAIN) mp = fmaxf(mp, fmaxf(fabsf(a[e]), fabsf(b[e])));
         }
-        rht16_block(a, sign_bits);
-        rht16_block(b, sign_bits);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) m = fmaxf(m, fmaxf(fabsf(a[e]), fabsf(b[e])));
+        m = fmaxf(m, fmaxf(rht16_absmax_unscaled(a, sign_bits),
+                           rht16_absmax_unscaled(b, sign_bits)));
       } else {
         float a[16];
 #pragma unroll
@@ -719,13 +717,11 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
           a[e] = __uint_as_float(wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w);
           if (PLAIN) mp = fmaxf(mp, fabsf(a[e]));
         }
-        rht16_block(a, sign_bits);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(a[e]));
+        m = fmaxf(m, rht16_absmax_unscaled(a, sign_bits));
       }
     }
   }
-  m = block_max(m, red);
+  m = block_max(__fmul_rn(m, 0.25f), red);  // the transform's x 1/4, on the maximum
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
   if (PLAIN) {
     mp = block_max(mp, red);
@@ -773,11 +769,9 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_row_kernel(const QParam
       v[e] = lo[e];
       v[8 + e] = hi[e];
     }
-    rht16_block(v, sign_bits);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+    m = fmaxf(m, rht16_absmax_unscaled(v, sign_bits));
   }
-  m = block_max(m, red);
+  m = block_max(__fmul_rn(m, 0.25f), red);  // the transform's x 1/4, on the maximum
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
 

@@ -82,8 +82,7 @@ NVFP4_DEV void tile_put(uint16_t* tile, int lane, int j, uint4 v) {
 }
 
 // Columns 2 lane and 2 lane + 1 of the warp's tile: max |x| into mp and the
-// 16-point transform of each (signs, butterfly stages h = 1, 2, 4, 8) into
-// mr as max |sum| before the final x 1/4.
+// 16-point transform of each into mr as max |sum| before the final x 1/4.
 NVFP4_DEV void column_amax(const uint16_t* tile, int lane, uint32_t sign_bits, float& mp,
                            float& mr) {
   float a[16], b[16];
@@ -94,17 +93,7 @@ NVFP4_DEV void column_amax(const uint16_t* tile, int lane, uint32_t sign_bits, f
     b[e] = __uint_as_float(w & 0xFFFF0000u);
     mp = fmaxf(mp, fmaxf(fabsf(a[e]), fabsf(b[e])));
   }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if ((sign_bits >> i) & 1u) {
-      a[i] = -a[i];
-      b[i] = -b[i];
-    }
-  }
-  butterfly_local<16>(a);
-  butterfly_local<16>(b);
-#pragma unroll
-  for (int e = 0; e < 16; ++e) mr = fmaxf(mr, fmaxf(fabsf(a[e]), fabsf(b[e])));
+  mr = fmaxf(mr, fmaxf(rht16_absmax_unscaled(a, sign_bits), rht16_absmax_unscaled(b, sign_bits)));
 }
 
 // The transform's x 1/4 on the maximum instead of on every sum: rounding is
