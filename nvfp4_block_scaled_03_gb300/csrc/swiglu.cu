@@ -19,6 +19,7 @@
 // transforms in registers, the quantiser's own arithmetic.
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -244,13 +245,21 @@ __global__ void __launch_bounds__(kThreads) swiglu_amax_finalize_kernel(const fl
 }
 
 // Persistent grid: a multiple of the SM count (as many CTAs per SM as fit,
-// within one set's partial slots), no more CTAs than warp tiles need.
-template <typename K>
-int grid_for(K kernel, int64_t tiles, int sms) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+// within one set's partial slots), no more CTAs than warp tiles need.  The
+// CTAs that fit per SM are looked up once per kernel and device.
+template <auto KERN>
+int grid_for(int64_t tiles, int sms) {
+  static std::atomic<int> fit[64];  // one cache per kernel
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int per_sm = fit[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KERN, kThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    fit[dev].store(per_sm, std::memory_order_relaxed);
+  }
   per_sm = std::max(1, std::min(per_sm, kSetStride / std::max(sms, 1)));
   const int64_t want = std::max<int64_t>(1, (tiles + kWarps - 1) / kWarps);
   return (int)std::min<int64_t>(std::min<int64_t>(want, (int64_t)sms * per_sm), kSetStride);
@@ -286,13 +295,13 @@ nvfp4_status swiglu_fwd_impl(const void* G, const void* U, void* H, int64_t rows
   int grid;
   AmaxDst out{};
   if (rht) {
-    grid = grid_for(swiglu_fwd_kernel<true>, tiles, dev.sm_count);
+    grid = grid_for<swiglu_fwd_kernel<true>>(tiles, dev.sm_count);
     swiglu_fwd_kernel<true><<<grid, kThreads, 0, stream>>>(g, u, h, rows, cols,
                                                            seed, pp);
     out.dst[0][0] = amax_row;
     out.dst[1][0] = amax_col;
   } else {
-    grid = grid_for(swiglu_fwd_kernel<false>, tiles, dev.sm_count);
+    grid = grid_for<swiglu_fwd_kernel<false>>(tiles, dev.sm_count);
     swiglu_fwd_kernel<false><<<grid, kThreads, 0, stream>>>(g, u, h, rows, cols, 0, pp);
     out.dst[0][0] = amax_row;
     out.dst[0][1] = amax_col;
@@ -329,13 +338,13 @@ nvfp4_status swiglu_bwd_impl(const void* dH, const void* G, const void* U, void*
   out.dst[0][0] = amax_dg_row;
   out.dst[1][0] = amax_du_row;
   if (rht) {
-    grid = grid_for(swiglu_bwd_kernel<true>, tiles, dev.sm_count);
+    grid = grid_for<swiglu_bwd_kernel<true>>(tiles, dev.sm_count);
     swiglu_bwd_kernel<true><<<grid, kThreads, 0, stream>>>(d, g, u, og, ou, rows, cols,
                                                            seed, pp);
     out.dst[2][0] = amax_dg_col;
     out.dst[3][0] = amax_du_col;
   } else {
-    grid = grid_for(swiglu_bwd_kernel<false>, tiles, dev.sm_count);
+    grid = grid_for<swiglu_bwd_kernel<false>>(tiles, dev.sm_count);
     swiglu_bwd_kernel<false><<<grid, kThreads, 0, stream>>>(d, g, u, og, ou, rows, cols, 0, pp);
     out.dst[0][1] = amax_dg_col;
     out.dst[1][1] = amax_du_col;
