@@ -36,7 +36,7 @@ METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roof
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM at
 # M=8192, N=14336, K=4096, from one ncu capture of that launch
-# (dram__bytes_read.sum 53.2 MB + dram__bytes_write.sum 188.1 MB); None once
+# (dram__bytes_read.sum 52.6 MB + dram__bytes_write.sum 188.2 MB); None once
 # the kernel changes after the capture.
 FPROP_TRAFFIC_BYTES = 52.615424e6 + 188.206080e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
