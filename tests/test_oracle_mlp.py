@@ -38,6 +38,35 @@ def test_swiglu_matches_autograd(orc):
         assert (diff <= 1).all() and (diff == 0).mean() > 0.999
 
 
+def test_swiglu_extreme_gates(orc):
+    """Gates across the range the outlier rows of the synthetic activations
+    reach (|g| up to 129, beyond where an FP32 e^-g overflows), against torch
+    autograd in FP64; and at g = 0 the closed forms silu(0) = 0 and
+    silu'(0) = 1/2, so dG = dH * u / 2 and dU = 0 there."""
+    gv = np.array([-129.0, -100.0, -90.5, -89.0, -88.5, -60.0, -20.0, -1.0, 0.0, 1.0, 20.0,
+                   60.0, 89.0, 129.0], np.float32)
+    g = np.repeat(syn.f32_to_bf16_bits(gv), 3)
+    u = np.tile(syn.f32_to_bf16_bits(np.array([0.875, -1.25, 3.0], np.float32)), len(gv))
+    dh = np.tile(syn.f32_to_bf16_bits(np.array([1.0, -0.5, 2.0], np.float32)), len(gv))
+    gt = torch.tensor(_f64(g), requires_grad=True)
+    ut = torch.tensor(_f64(u), requires_grad=True)
+    h = torch.nn.functional.silu(gt) * ut
+    h.backward(torch.tensor(_f64(dh)))
+    got_h = orc.swiglu_fwd(g, u)
+    got_dg, got_du = orc.swiglu_bwd(dh, g, u)
+    for got, ref in ((got_h, h.detach().numpy()), (got_dg, gt.grad.numpy()),
+                     (got_du, ut.grad.numpy())):
+        diff = np.abs(got.astype(np.int32) - orc.bf16_round_f64(ref).astype(np.int32))
+        assert (diff <= 1).all()
+    # the silu(g) u of the outlier gates is a normal bf16 number, not zero
+    i = int(np.where(gv == -89.0)[0][0]) * 3
+    assert 1e-38 < abs(_f64(got_h[i:i + 1])[0]) < 1e-36
+    z = int(np.where(gv == 0.0)[0][0]) * 3
+    np.testing.assert_array_equal(_f64(got_h[z:z + 3]), 0.0)
+    np.testing.assert_array_equal(_f64(got_du[z:z + 3]), 0.0)
+    np.testing.assert_array_equal(_f64(got_dg[z:z + 3]), _f64(dh[z:z + 3]) * _f64(u[z:z + 3]) / 2)
+
+
 def _torch_mlp(X, Wg, Wu, Wd, dY):
     Xt = torch.tensor(_f64(X), requires_grad=True)
     ws = [torch.tensor(w.astype(np.float64), requires_grad=True) for w in (Wg, Wu, Wd)]
