@@ -84,3 +84,60 @@ def test_mlp_sizes(lib):
     assert s.value > 2 * 256 * 512 * 2 and w.value > 4 * 256 * 512 * 2
     assert lib.nvfp4_mlp_sizes(C.c_int64(100), C.c_int64(256), C.c_int64(512), C.byref(s),
                                C.byref(w)) == 2
+
+
+def test_mx_sizes_follow_the_header_rule(lib):
+    """nvfp4_mx_sizes against the layout rule the header states: codes of
+    out_rows x out_cols at 4 or 8 bits, one scale byte per 32 outputs, and the
+    MMA layout padded to 128 rows x 4 scale columns per 512-byte atom."""
+    sz = C.c_size_t
+
+    def sizes(rows, cols, mode, fmt):
+        c, s, w = sz(), sz(), sz()
+        st = lib.nvfp4_mx_sizes(C.c_int64(rows), C.c_int64(cols), C.c_int32(mode),
+                                C.c_int32(fmt), C.byref(c), C.byref(s), C.byref(w))
+        return st, c.value, s.value, w.value
+
+    def atoms(orows, ocols):
+        return -(-orows // 128) * -(-(ocols // 32) // 4) * 512
+
+    for rows, cols in ((64, 96), (333, 1056), (1, 32)):
+        for fmt, bits in ((0, 4), (1, 8)):
+            assert sizes(rows, cols, 0, fmt) == (0, rows * cols * bits // 8, rows * cols // 32,
+                                                 atoms(rows, cols))
+    for rows, cols in ((64, 136), (320, 1000)):
+        for fmt, bits in ((0, 4), (1, 8)):
+            assert sizes(rows, cols, 1, fmt) == (0, rows * cols * bits // 8, rows * cols // 32,
+                                                 atoms(cols, rows))
+    assert sizes(64, 48, 0, 0)[0] == 2      # 48 columns: not whole 32-element blocks
+    assert sizes(40, 64, 1, 1)[0] == 2      # 40 rows along the column blocks
+    assert lib.nvfp4_mx_sizes(C.c_int64(64), C.c_int64(64), 0, 0, None, None, None) == 0
+
+
+def test_swiglu_argument_errors_return_before_any_launch(lib):
+    """The SwiGLU entry points check their arguments on the host: unknown
+    flags and NULL pointers (invalid argument), rows not a multiple of 16
+    (shape), a short workspace, and misaligned tensors -- all before touching
+    a device, so the fake addresses below are never dereferenced."""
+    vp, i64, u32, u64, sz = C.c_void_p, C.c_int64, C.c_uint32, C.c_uint64, C.c_size_t
+    lib.nvfp4_swiglu_workspace_bytes.restype = sz
+    lib.nvfp4_swiglu_fwd.argtypes = [vp, vp, vp, i64, i64, u32, u64, vp, vp, vp, sz, vp]
+    lib.nvfp4_swiglu_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, u32, u64, vp, vp, vp, vp,
+                                     vp, sz, vp]
+    wsb = lib.nvfp4_swiglu_workspace_bytes()
+    assert wsb >= 16 and wsb % 16 == 0
+    t, a, ws = 0x10000, 0x20000, 0x30000        # 16-byte aligned fake addresses
+    fwd, bwd = lib.nvfp4_swiglu_fwd, lib.nvfp4_swiglu_bwd
+    assert fwd(t, t, t, 32, 64, 0x80, 0, a, a, ws, wsb, None) == 1    # unknown flag
+    assert fwd(t, t, None, 32, 64, 0, 0, a, a, ws, wsb, None) == 1    # NULL output
+    assert fwd(t, t, t, 32, 64, 0, 0, a, None, ws, wsb, None) == 1    # NULL amax
+    assert fwd(t, t, t, 40, 64, 1, 0, a, a, ws, wsb, None) == 2       # rows % 16
+    assert fwd(t, t, t, 32, 60, 1, 0, a, a, ws, wsb, None) == 2       # cols % 8
+    assert fwd(t, t, t, 32, 64, 1, 0, a, a, ws, wsb - 16, None) == 5  # workspace
+    assert fwd(t + 8, t, t, 32, 64, 1, 0, a, a, ws, wsb, None) == 3   # misaligned G
+    assert bwd(t, t, t, t, t, 32, 64, 2, 0, a, a, a, a, ws, wsb, None) == 1   # SR: not a flag here
+    assert bwd(t, t, t, t, None, 32, 64, 0, 0, a, a, a, a, ws, wsb, None) == 1
+    assert bwd(t, t, t, t, t, 24, 64, 0, 0, a, a, a, a, ws, wsb, None) == 2
+    assert bwd(t, t, t, t, t, 32, 64, 0, 0, a, a, a, a, None, wsb, None) == 5
+    assert bwd(t, t, t, t, t + 4, 32, 64, 0, 0, a, a, a, a, ws, wsb, None) == 3
+    assert bwd(t, t, t, t, t, 32, 64, 0, 0, a, a, a + 2, a, ws, wsb, None) == 3  # amax not 4-aligned
