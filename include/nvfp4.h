@@ -177,15 +177,18 @@ nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t c
  * every GPU that loads the library until the process exits.  The caller still
  * passes x and the output buffers of `out`, exactly as for nvfp4_quantize, and
  * gets the same results.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  The call itself allocates and frees nothing.  All calls share the
- * one array: calls that can overlap on the GPU (different streams, no
- * ordering between them) race and must not be issued that way.  Each call's
- * amax pass rewrites every partial its quantise pass reads, so nothing needs
- * clearing between calls.  Returns NVFP4_ERR_WORKSPACE if the device has more
- * SMs than the array can hold partials for (4 per SM, so above 256 SMs);
- * otherwise the same statuses as nvfp4_quantize. */
+ * Every call made outside stream capture looks up the array's device address
+ * on the current device (after a cudaDeviceReset the array may move); a call
+ * made while `stream` is being captured reuses the address the last
+ * uncaptured call on that device found, so make the first call on a device
+ * before any stream capture.  The call itself allocates and frees nothing.
+ * All calls share the one array: calls that can overlap on the GPU
+ * (different streams, no ordering between them) race and must not be issued
+ * that way.  Each call's amax pass rewrites every partial its quantise pass
+ * reads, so nothing needs clearing between calls.  The array holds the
+ * partial maxima of the largest amax grid the library launches (1024 CTAs),
+ * so every device and shape nvfp4_quantize accepts is accepted; the statuses
+ * are those of nvfp4_quantize. */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
                                     int64_t ld, int32_t mode, uint32_t flags, uint64_t seed,
                                     uint64_t offset, nvfp4_tensor* out, nvfp4_stream stream);
@@ -286,7 +289,7 @@ enum {
   NVFP4_TILE_128X128 = 1,       /* one SM per 128 x 128 tile                               */
   NVFP4_TILE_128X256 = 2,       /* one SM per 128 x 256 tile                               */
   NVFP4_TILE_PAIR_256X256 = 3,  /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */
-  NVFP4_TILE_128X256_MC2 = 4,   /* one SM per 128 x 256 tile, clusters of two sharing B    */
+  /* 4 is retired (rejected with NVFP4_ERR_INVALID_ARG)                                    */
   NVFP4_TILE_128X256_K128 = 5   /* one SM per 128 x 256 tile, 8 stages of K = 128          */
 };
 

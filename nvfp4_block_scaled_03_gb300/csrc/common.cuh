@@ -409,25 +409,6 @@ NVFP4_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t b
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
-// TMA tile load multicast to the same shared-memory offset (and mbarrier
-// offset) of every CTA in `mask`.
-NVFP4_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
-                              int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-// Arrive on the same-offset mbarrier of every CTA in `mask` when this thread's
-// prior tcgen05 operations complete (single-SM MMAs).
-NVFP4_DEV void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 // 5-D variant (coordinates 0, 0, 0, x3, x4) completing on a pair barrier.
 NVFP4_DEV void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
                                 int32_t x3, int32_t x4) {

@@ -100,11 +100,10 @@ NVFP4_DEV void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Bounded wait for a kernel launched in clusters of MC CTAs: a timeout also
-// raises the peer CTA's abort flag.
-template <int MC>
-NVFP4_DEV bool wait_bounded_mc(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                               uint32_t peer_abort_addr, unsigned int code) {
+// Bounded wait of the single-SM kernel: on expiry it raises the CTA's abort
+// flag and records `code` in the error word.
+NVFP4_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                            unsigned int code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -112,7 +111,6 @@ NVFP4_DEV bool wait_bounded_mc(uint32_t bar, uint32_t parity, volatile int* abor
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
       *abort_flag = 1;
-      if (MC == 2) st_cluster_u32(peer_abort_addr, 1u);
       atomicCAS(&g_gemm_error, 0u, code);
       return false;
     }
@@ -189,7 +187,7 @@ NVFP4_DEV void prefetch_l2_row(const void* p, int bytes) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(c + o)));
 }
 
-template <int BN, int STAGES, int DMODE, int MC, int BKB>
+template <int BN, int STAGES, int DMODE, int BKB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
@@ -210,19 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = (args.K + 2 * BKB - 1) / (2 * BKB);
-  // MC == 2: the two CTAs of a cluster take vertically adjacent tiles (same
-  // n_blk) and share their B tile -- each loads half and multicasts it.
-  const uint32_t rank = MC == 2 ? cluster_ctarank() : 0u;
-  const int num_mu = (args.num_m_blk + MC - 1) / MC;  // M units of MC tiles
+  const int num_mu = args.num_m_blk;
   const int num_units = num_mu * args.num_n_blk;
-  const int unit0 = blockIdx.x / MC, unit_step = gridDim.x / MC;
-  const uint32_t peer_abort =
-      MC == 2 ? mapa_shared(smem_u32(smem + L::offMisc + 4), rank ^ 1u) : 0u;
+  const int unit0 = blockIdx.x, unit_step = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MC);  // the MMA of every CTA that reads stage s
+      mbar_init(empty_bar(s), 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -236,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (MC == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -250,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < STAGES; ++i) armed[i] = -1;
       bool ok = true;
       for (int unit = unit0; ok && unit < num_units; unit += unit_step) {
-        const int m_blk = (unit % num_mu) * MC + (int)rank, n_blk = unit / num_mu;
+        const int m_blk = unit % num_mu, n_blk = unit / num_mu;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded_mc<MC>(empty_bar(s), ph ^ 1u, abort_flag, peer_abort, 0x10u)) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, 0x10u)) {
             ok = false;
             break;
           }
@@ -263,11 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full_bar(s), L::kA + L::kB + sf_bytes);
           armed[s] = (int)ph;
           tma_load_2d(sbase + L::offA + s * L::kA, &tmA, full_bar(s), kb * BKB, m_blk * kBM);
-          if (MC == 2)  // this CTA's half of the shared B tile, to both CTAs
-            tma_load_2d_mc(sbase + L::offB + s * L::kB + rank * (L::kB / 2), &tmB, full_bar(s),
-                           kb * BKB, n_blk * BN + (int)rank * (BN / 2), (uint16_t)3);
-          else
-            tma_load_2d(sbase + L::offB + s * L::kB, &tmB, full_bar(s), kb * BKB, n_blk * BN);
+          tma_load_2d(sbase + L::offB + s * L::kB, &tmB, full_bar(s), kb * BKB, n_blk * BN);
           bulk_load(sbase + L::offSFA + s * L::kSFA,
                     args.sfa + ((int64_t)m_blk * args.kg + kb * kAt) * 512,
                     natoms * 512u, full_bar(s));
@@ -293,13 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s = 0, ph = 0, acc_ph = 0;
       bool ok = true, issued = false;
       for (int unit = unit0; ok && unit < num_units; unit += unit_step) {
-        if (!wait_bounded_mc<MC>(acc_empty, acc_ph ^ 1u, abort_flag, peer_abort, 0x20u)) {
+        if (!wait_bounded(acc_empty, acc_ph ^ 1u, abort_flag, 0x20u)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded_mc<MC>(full_bar(s), ph, abort_flag, peer_abort, 0x21u)) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, 0x21u)) {
             ok = false;
             break;
           }
@@ -323,8 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sfa_t + 4 * j, sfb_t + j * (BN / 32), (kb | j) != 0 ? 1u : 0u);
           }
           issued = true;
-          if (MC == 2) tc_commit_mc(empty_bar(s), 3);  // both CTAs wrote into this stage
-          else tc_commit(empty_bar(s));
+          tc_commit(empty_bar(s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -346,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
     uint32_t acc_ph = 0;
     for (int unit = unit0; unit < num_units; unit += unit_step) {
-      const int m_blk = (unit % num_mu) * MC + (int)rank, n_blk = unit / num_mu;
-      if (!wait_bounded_mc<MC>(acc_full, acc_ph, abort_flag, peer_abort, 0x30u)) break;
+      const int m_blk = unit % num_mu, n_blk = unit / num_mu;
+      if (!wait_bounded(acc_full, acc_ph, abort_flag, 0x30u)) break;
       tc_fence_after();
       uint32_t r[kChunks][32];
 #pragma unroll
@@ -369,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (MC == 2) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -870,11 +856,11 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int DMODE, int MC, int BKB>
+template <int BN, int STAGES, int DMODE, int BKB>
 nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int sms,
                     cudaStream_t stream) {
   using L = Smem<BN, STAGES, BKB>;
-  auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE, MC, BKB>;
+  auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE, BKB>;
   static bool configured = false;  // attribute is per function; setting it twice is harmless
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
@@ -882,38 +868,21 @@ nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs
       return NVFP4_ERR_CUDA;
     configured = true;
   }
-  const int units = ((a.num_m_blk + MC - 1) / MC) * a.num_n_blk;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::kAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = MC;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(MC * (sms / MC));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / MC;
-    max_clusters = std::min(n, sms / MC);
-  }
-  cfg.gridDim = dim3(MC * std::min(units, max_clusters));
-  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, a) != cudaSuccess) return NVFP4_ERR_CUDA;
+  // persistent grid: one CTA per SM (tensor memory and shared memory admit
+  // one), at most one per output tile
+  const int units = a.num_m_blk * a.num_n_blk;
+  kern<<<std::min(units, sms), kThreads, L::kAlloc, stream>>>(ma, mb, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int MC, int BKB>
+template <int BN, int STAGES, int BKB>
 nvfp4_status launch_mode(int d_mode, const CUtensorMap& ma, const CUtensorMap& mb,
                          const GemmArgs& a, int sms, cudaStream_t s) {
   switch (d_mode) {
-    case NVFP4_D_BF16: return launch<BN, STAGES, NVFP4_D_BF16, MC, BKB>(ma, mb, a, sms, s);
+    case NVFP4_D_BF16: return launch<BN, STAGES, NVFP4_D_BF16, BKB>(ma, mb, a, sms, s);
     case NVFP4_D_F32_ACCUM:
-      return launch<BN, STAGES, NVFP4_D_F32_ACCUM, MC, BKB>(ma, mb, a, sms, s);
-    default: return launch<BN, STAGES, NVFP4_D_BF16_ADD_C, MC, BKB>(ma, mb, a, sms, s);
+      return launch<BN, STAGES, NVFP4_D_F32_ACCUM, BKB>(ma, mb, a, sms, s);
+    default: return launch<BN, STAGES, NVFP4_D_BF16_ADD_C, BKB>(ma, mb, a, sms, s);
   }
 }
 
@@ -963,7 +932,8 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   if (a_view < 0 || a_view > 1 || b_view < 0 || b_view > 1) return NVFP4_ERR_INVALID_ARG;
   if (d_mode < NVFP4_D_BF16 || d_mode > NVFP4_D_BF16_ADD_C) return NVFP4_ERR_INVALID_ARG;
   if (d_mode == NVFP4_D_BF16_ADD_C && !C) return NVFP4_ERR_INVALID_ARG;
-  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_128X256_K128) return NVFP4_ERR_INVALID_ARG;
+  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_128X256_K128 || tile == 4)
+    return NVFP4_ERR_INVALID_ARG;  // 4: a retired configuration
   const void* a_codes = a_view ? A->codes_t : A->codes;
   const void* a_sf = a_view ? A->scales_t : A->scales;
   const void* b_codes = b_view ? B->codes_t : B->codes;
@@ -1022,17 +992,15 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     return launch_pair_mode<4>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
   }
   const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
-  const int mc = tile == NVFP4_TILE_128X256_MC2 ? 2 : 1;
   const int bkb = tile == NVFP4_TILE_128X256_K128 ? 64 : 128;  // stage K bytes per row
   if (!make_code_map(&ma, a_codes, M, K / 2, kBM, bkb) ||
-      !make_code_map(&mb, b_codes, N, K / 2, bn / mc, bkb))
+      !make_code_map(&mb, b_codes, N, K / 2, bn, bkb))
     return NVFP4_ERR_CUDA;
   a.num_m_blk = (int)((M + kBM - 1) / kBM);
   a.num_n_blk = (int)((N + bn - 1) / bn);
-  if (bkb == 64) return launch_mode<256, 8, 1, 64>(d_mode, ma, mb, a, dev.sm_count, stream);
-  if (mc == 2) return launch_mode<256, 4, 2, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
-  if (bn == 256) return launch_mode<256, 4, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
-  return launch_mode<128, 6, 1, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
+  if (bkb == 64) return launch_mode<256, 8, 64>(d_mode, ma, mb, a, dev.sm_count, stream);
+  if (bn == 256) return launch_mode<256, 4, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
+  return launch_mode<128, 6, 128>(d_mode, ma, mb, a, dev.sm_count, stream);
 }
 
 // D bf16 [M, N] = A . B^T for MX operands (codes K-major; scales in the MMA

@@ -976,6 +976,8 @@ nvfp4_status quant_read_error(unsigned int* code) {
 namespace {
 
 constexpr int kNoAllocPartials = kMaxPartials;  // 1024 floats: 4 KB per device
+// every amax grid is capped at kMaxPartials CTAs, one partial each
+static_assert(kNoAllocPartials >= kMaxPartials, "the array holds every partial maximum");
 // Lives on every device that loads the library, until the process exits.
 // In host code this name is only a stand-in: kernels receive the device
 // address obtained with cudaGetSymbolAddress below.
@@ -984,14 +986,18 @@ static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64] = {};
 
-// Device address of the array on the current device, looked up once per
-// device (the first call on a device does this; make that first call before
-// any stream capture).
-nvfp4_status noalloc_scratch(void** addr) {
+// Device address of the array on the current device.  Outside stream capture
+// it is looked up on every call (cudaDeviceReset reloads the module, and the
+// array may then sit at another address); during capture the address found
+// by the last call outside capture on this device is used, so the first call
+// on a device must come before any capture.
+nvfp4_status noalloc_scratch(cudaStream_t stream, void** addr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return NVFP4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_noalloc_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return NVFP4_ERR_CUDA;
     g_noalloc_addr[dev] = p;
@@ -1017,10 +1023,8 @@ extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t in_dtype, 
   DeviceInfo dev;
   nvfp4_status st = current_device(&dev);
   if (st != NVFP4_OK) return st;
-  // the amax pass writes one partial per CTA: reject what the array cannot hold
-  if ((int64_t)dev.sm_count * 4 > kNoAllocPartials) return NVFP4_ERR_WORKSPACE;
   void* scratch = nullptr;
-  st = noalloc_scratch(&scratch);
+  st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
   if (st != NVFP4_OK) return st;
   // every partial the quantise pass reads is written by this call's amax pass
   // first, so nothing needs clearing between calls
