@@ -2,9 +2,10 @@
 
 One step = one pass of the whole path over the Llama-3-8B MLP up/gate
 projection (M = 8192 tokens, K = 4096, N = 14336, synthetic seeded inputs
-resident in HBM): quantise X (1x16 RNE for FPROP, column-wise 1x16 + RHT for
-WGRAD), W (16x16 RNE + transpose), dY (1x16 SR for DGRAD, column-wise RHT+SR
-for WGRAD), then the FPROP, DGRAD and WGRAD block-scaled GEMMs to BF16.
+resident in HBM): quantise X (1x16 RNE for FPROP and column-wise 1x16 + RHT
+for WGRAD, from one read after its amax pass), W (16x16 RNE + transpose), dY
+(1x16 SR for DGRAD and column-wise RHT+SR for WGRAD, likewise), then the
+FPROP, DGRAD and WGRAD block-scaled GEMMs to BF16.
 
 Prints one JSON line: value = GEMM FLOPs of the step (3 x 2MNK) / step time,
 aggregated over ranks; plus the GEMM roofline (tensor-bound, FP4 peak =
@@ -208,40 +209,41 @@ class Layer:
         self.ws = torch.empty(nv.quantize_sizes(M, K, 0)[3], dtype=torch.uint8, device=device)
         self.out_host = {k: torch.empty(self.sets[0][k].shape, dtype=torch.bfloat16).pin_memory()
                          for k in ("Y", "dX", "dW")}
-        # launches per step: one-read amax of X and of dY (2 each), 4 given-amax
-        # quantise passes, W's quantiser (amax pass + quantise pass), 3 GEMMs
-        self.launches_per_step = 2 * 2 + 4 + 2 + 3
-        self.names = ["q_x_amax", "q_x_row", "q_x_col_rht", "q_w_16x16", "q_dy_amax",
-                      "q_dy_row_sr", "q_dy_col_rht_sr", "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
+        # launches per step: one-read amax of X and of dY (2 each), one-read
+        # row + column quantise pass of each, W's quantiser (amax pass +
+        # quantise pass), 3 GEMMs
+        self.launches_per_step = 2 * 2 + 2 + 2 + 3
+        self.names = ["q_x_amax", "q_x_rowcol_rht", "q_w_16x16", "q_dy_amax",
+                      "q_dy_rowcol_rht_sr", "gemm_fprop", "gemm_dgrad", "gemm_wgrad"]
 
     def flops(self):
         return 3 * 2.0 * self.M * self.N * self.K
 
     def quant_bytes(self):
-        """Algorithmic bytes of the five quantiser calls (amax pre-pass
-        excluded): read the bf16 input once, write codes and scales."""
+        """Algorithmic bytes of the step's quantisation (amax pre-passes
+        excluded): each bf16 input read once; X and dY each write a row-wise
+        and a column-wise operand (codes 1/2 B and scales 1/16 B per element,
+        twice), W its codes in both layouts and two 1/256 B scale copies."""
         M, K, N = self.M, self.K, self.N
         b = 0
-        for rows, cols, t in ((M, K, 1), (M, K, 1), (N, K, 2), (M, N, 1), (M, N, 1)):
-            elts = rows * cols
-            b += 2 * elts + elts / 2 * t + (elts / 16 if t == 1 else 2 * elts / 256)
+        for rows, cols in ((M, K), (M, N)):
+            b += rows * cols * (2 + 2 * (0.5 + 1 / 16))
+        b += N * K * (2 + 1.0 + 2 / 256)
         return b
 
     def step(self, events=None, buf=0):
         nv, d = self.nv, self.sets[buf]
-        G = nv.AMAX_GIVEN
         calls = [
             lambda: nv.nvfp4_amax(d["X"], self.qX.amax, self.qXc.amax, seed=0, workspace=self.ws),
-            lambda: nv.nvfp4_quantize(d["X"], nv.ROW_1X16, G, out=self.qX),
-            lambda: nv.nvfp4_quantize(d["X"], nv.COL_1X16, nv.RHT | G, seed=0, out=self.qXc),
+            lambda: nv.nvfp4_quantize_rowcol(d["X"], 0, nv.RHT, seed=0, row_out=self.qX,
+                                             col_out=self.qXc),
             lambda: nv.nvfp4_quantize(d["W"], nv.BLOCK_16X16, nv.EMIT_T, out=self.qW,
                                       workspace=self.ws),
             lambda: nv.nvfp4_amax(d["dY"], self.qdY.amax, self.qdYc.amax, seed=0,
                                   workspace=self.ws),
-            lambda: nv.nvfp4_quantize(d["dY"], nv.ROW_1X16, nv.SR | G, seed=0, offset=0,
-                                      out=self.qdY),
-            lambda: nv.nvfp4_quantize(d["dY"], nv.COL_1X16, nv.RHT | nv.SR | G, seed=0, offset=1,
-                                      out=self.qdYc),
+            lambda: nv.nvfp4_quantize_rowcol(d["dY"], nv.SR, nv.RHT | nv.SR, seed=0,
+                                             row_offset=0, col_offset=1, row_out=self.qdY,
+                                             col_out=self.qdYc),
             lambda: nv.nvfp4_gemm(self.qX, self.qW, out=d["Y"]),
             lambda: nv.nvfp4_gemm(self.qdY, self.qW, b_view=1, out=d["dX"]),
             lambda: nv.nvfp4_gemm(self.qdYc, self.qXc, out=d["dW"]),
@@ -701,6 +703,27 @@ def run_quant_sweep(args):
                 "frac_quantise": round(nbytes / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                 "ms_quantise_min": round(t_q_min, 4)})
             del q
+        # the one-read row + column forms (X: RNE / RHT; dY: SR / RHT + SR),
+        # amaxes given: read once, two operands written
+        for name, rf, cf, kind in (("rowcol_rne_rht", 0, nv.RHT, "act"),
+                                   ("rowcol_sr_rht_sr", nv.SR, nv.RHT | nv.SR, "grad")):
+            x = data[kind]
+            qr = nv.alloc_qtensor(rows, cols, nv.ROW_1X16, device=device)
+            qc = nv.alloc_qtensor(rows, cols, nv.COL_1X16, device=device)
+            nv.nvfp4_amax(x, qr.amax, qc.amax, seed=0, workspace=ws)
+
+            def given_rc():
+                nv.nvfp4_quantize_rowcol(x, rf, cf, seed=0, row_offset=0, col_offset=1,
+                                         row_out=qr, col_out=qc)
+            t_q, t_q_min = _timed(given_rc, reps, flush_l2)
+            nbytes = 2 * elts + 2 * (elts / 2 + elts / 16)
+            results.append({
+                "shape": [rows, cols], "form": name, "algorithmic_bytes": int(nbytes),
+                "ms_quantise": round(t_q, 4),
+                "gbs_quantise": round(nbytes / (t_q * 1e-3) / 1e9, 1),
+                "frac_quantise": round(nbytes / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "ms_quantise_min": round(t_q_min, 4)})
+            del qr, qc
         del data, ws
         torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -709,7 +732,7 @@ def run_quant_sweep(args):
         "metric": "NVFP4 quantiser GB/s on algorithmic bytes", "unit": "GB/s",
         "higher_is_better": True, "n_gpus": 1, "dtype": "bf16 in, nvfp4 out", "data": DATA,
         "config": {"workload": "quantiser sweep: tokens {8192, 32768} x {4096, 14336}, six "
-                               "quantiser forms",
+                               "quantiser forms and the two one-read row + column forms",
                    "reps": reps, "l2": "flushed before every timed call (untimed)"},
         "peak_gbs": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
         "results": results, "clocks": clk, "impl": "ours"}), flush=True)

@@ -106,6 +106,25 @@ nvfp4_status nvfp4_device_check(int device);
  * if it was set, NVFP4_ERR_CUDA if the stream reported an error. */
 nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream);
 
+/* Failure injection for tests of the bounded waits; the pages have no
+ * counterpart (they describe no failure handling).  While a bit of
+ * stall_mask is set, the producer of every launch of that kernel family
+ * issues no loads, so the consumers' first pipeline wait runs out; nothing is
+ * in flight when the kernel gives up, and it returns after recording the
+ * timeout (nvfp4_check_device_errors then reports NVFP4_ERR_DEVICE_TIMEOUT):
+ *   NVFP4_STALL_QUANTIZE  the quantise passes of nvfp4_quantize
+ *   NVFP4_STALL_GEMM      the single-SM GEMM kernel (NVFP4_TILE_128X128 /
+ *                         128X256 / 128X256_K128; the CTA-pair kernel is
+ *                         not affected)
+ * wait_limit_ns sets how long those kernels' pipeline waits last before they
+ * give up (0: the default, 2 s); the waits that drain copies and MMAs
+ * already issued keep their own 2 s limit.  Synchronises the device, then
+ * applies to later launches until changed; call it with nothing of this
+ * library in flight.  Returns NVFP4_ERR_INVALID_ARG for unknown bits,
+ * NVFP4_ERR_CUDA if the device cannot be reached. */
+enum { NVFP4_STALL_QUANTIZE = 1u, NVFP4_STALL_GEMM = 2u };
+nvfp4_status nvfp4_debug_inject(uint32_t stall_mask, uint64_t wait_limit_ns);
+
 /* ---------------------------------------------------------------------- */
 /* Quantiser                                                               */
 /* ---------------------------------------------------------------------- */
@@ -167,6 +186,28 @@ nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64
 nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
                         uint64_t seed, float* amax_plain, float* amax_rht, void* workspace,
                         size_t workspace_bytes, nvfp4_stream stream);
+
+/* Both quantisations a training step makes of one bf16 activation or
+ * gradient x [rows, cols] (leading dim ld), from one read of x -- bit for bit
+ * what two nvfp4_quantize calls give ("NVFP4 pretraining recipe", bullets
+ * 1-5: the FPROP / DGRAD operand is quantised row-wise, the WGRAD operand
+ * column-wise with the RHT on the WGRAD inputs only, SR on gradients):
+ *   row_out: nvfp4_quantize(x, ROW_1X16, row_flags, seed, row_offset)
+ *   col_out: nvfp4_quantize(x, COL_1X16, col_flags, seed, col_offset)
+ * row_flags: NVFP4_AMAX_GIVEN, optionally | NVFP4_SR; col_flags:
+ * NVFP4_AMAX_GIVEN, optionally | NVFP4_RHT | NVFP4_SR.  Both amaxes are given
+ * (*row_out->amax = max |x|, *col_out->amax = the column operand's amax, e.g.
+ * both from one nvfp4_amax call), so nothing needs a workspace.  Shapes:
+ * rows % 16 == 0, cols % 16 == 0.  x, the codes and scales buffers 16-byte
+ * aligned, ld * 2 a multiple of 16; bf16 input only.  One kernel launch on
+ * `stream`; nothing is allocated.  Returns NVFP4_ERR_INVALID_ARG (a NULL
+ * pointer, fp32 input, a flag outside those above or AMAX_GIVEN missing),
+ * _SHAPE, _ALIGN, _ARCH, _CUDA. */
+nvfp4_status nvfp4_quantize_rowcol(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                   int64_t ld, uint32_t row_flags, uint32_t col_flags,
+                                   uint64_t seed, uint64_t row_offset, uint64_t col_offset,
+                                   nvfp4_tensor* row_out, nvfp4_tensor* col_out,
+                                   nvfp4_stream stream);
 
 /* nvfp4_quantize without a workspace argument; the paper has no counterpart
  * to this entry point.  It is for callers that cannot provide device scratch
@@ -368,6 +409,48 @@ nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, vo
 nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void* saved,
                            void* dX, float* dWg, float* dWu, float* dWd, void* workspace,
                            size_t workspace_bytes, nvfp4_stream stream);
+
+/* Where nvfp4_mlp_fwd / nvfp4_mlp_bwd keep the intermediates of one MLP
+ * step inside the caller's `saved` and workspace buffers, so a caller can
+ * read them after a call (to inspect or check each stage of the step); the
+ * same Figure 1 text passage as the MLP calls.  The bf16 tensors (row-major):
+ *   G, U       [M, F]  in saved      (gate and up projections, forward)
+ *   H          [M, F]  in workspace  (silu(G) * U, forward)
+ *   DH, DG, DU [M, F]  in workspace  (backward: dY Wd, the SwiGLU derivative)
+ *   DX_GATE    [M, D]  in workspace  (backward: bf16(dG Wg), which the
+ *                                     second DGRAD adds to dU Wu)
+ * Contents are those the last fwd (G, U, H) or bwd (the others) call wrote.
+ */
+enum {
+  NVFP4_MLP_G = 0, NVFP4_MLP_U = 1, NVFP4_MLP_H = 2, NVFP4_MLP_DH = 3, NVFP4_MLP_DG = 4,
+  NVFP4_MLP_DU = 5, NVFP4_MLP_DX_GATE = 6
+};
+/* *data = device address of tensor `which` inside saved / workspace (the
+ * buffer that holds it must not be NULL; the other may be), *rows, *cols its
+ * shape.  Returns NVFP4_ERR_SHAPE as nvfp4_mlp_sizes, NVFP4_ERR_INVALID_ARG for
+ * an unknown `which` or a NULL pointer.  Nothing is launched. */
+nvfp4_status nvfp4_mlp_tensor(int64_t M, int64_t D, int64_t F, const void* saved,
+                              const void* workspace, int32_t which, void** data, int64_t* rows,
+                              int64_t* cols);
+
+/* The quantised operands of the nine GEMMs (descriptors with rows x cols the
+ * logical K-major operand, as nvfp4_quantize fills them):
+ *   Q_WG, Q_WU [F, D], Q_WD [D, F]  in saved  16x16 with the transpose
+ *                                             (codes_t / scales_t)
+ *   Q_XC [D, M], Q_HC [F, M]        in saved  the forward's WGRAD operands
+ *   Q_X [M, D], Q_H [M, F]          in workspace (FPROP operands)
+ *   Q_DY [M, D], Q_DG, Q_DU [M, F]  in workspace (DGRAD operands, SR)
+ *   Q_DYC [D, M], Q_DGC, Q_DUC [F, M] in workspace (WGRAD operands)
+ * *out receives the pointers into the buffers; amax and s_dec point at the
+ * device floats the quantiser wrote.  Returns as nvfp4_mlp_tensor. */
+enum {
+  NVFP4_MLP_Q_WG = 16, NVFP4_MLP_Q_WU = 17, NVFP4_MLP_Q_WD = 18, NVFP4_MLP_Q_X = 19,
+  NVFP4_MLP_Q_XC = 20, NVFP4_MLP_Q_H = 21, NVFP4_MLP_Q_HC = 22, NVFP4_MLP_Q_DY = 23,
+  NVFP4_MLP_Q_DYC = 24, NVFP4_MLP_Q_DG = 25, NVFP4_MLP_Q_DGC = 26, NVFP4_MLP_Q_DU = 27,
+  NVFP4_MLP_Q_DUC = 28
+};
+nvfp4_status nvfp4_mlp_operand(int64_t M, int64_t D, int64_t F, const void* saved,
+                               const void* workspace, int32_t which, nvfp4_tensor* out);
 
 #ifdef __cplusplus
 }

@@ -61,12 +61,15 @@ def _load():
         "nvfp4_version": ([], C.c_int),
         "nvfp4_device_check": ([C.c_int], C.c_int),
         "nvfp4_check_device_errors": ([vp], C.c_int),
+        "nvfp4_debug_inject": ([u32, u64], C.c_int),
         "nvfp4_quantize_sizes": ([i64, i64, i32, u32, P(sz), P(sz), P(sz), P(sz)], C.c_int),
         "nvfp4_quantize": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp, sz, vp],
                            C.c_int),
         "nvfp4_quantize_noalloc": ([vp, i32, i64, i64, i64, i32, u32, u64, u64, P(Tensor), vp],
                                    C.c_int),
         "nvfp4_amax": ([vp, i32, i64, i64, i64, u64, vp, vp, vp, sz, vp], C.c_int),
+        "nvfp4_quantize_rowcol": ([vp, i32, i64, i64, i64, u32, u32, u64, u64, u64, P(Tensor),
+                                   P(Tensor), vp], C.c_int),
         "nvfp4_gemm": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, vp, sz, vp],
                        C.c_int),
         "nvfp4_gemm_ex": ([P(Tensor), i32, P(Tensor), i32, vp, i32, vp, i64, i64, i64, i32, vp],
@@ -81,6 +84,8 @@ def _load():
         "nvfp4_mlp_sizes": ([i64, i64, i64, P(sz), P(sz)], C.c_int),
         "nvfp4_mlp_fwd": ([P(MlpParams), vp, vp, vp, sz, vp, sz, vp], C.c_int),
         "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
+        "nvfp4_mlp_tensor": ([i64, i64, i64, vp, vp, i32, P(vp), P(i64), P(i64)], C.c_int),
+        "nvfp4_mlp_operand": ([i64, i64, i64, vp, vp, i32, P(Tensor)], C.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -215,6 +220,35 @@ def nvfp4_amax(x: torch.Tensor, amax_plain: torch.Tensor | None = None,
     _check(lib.nvfp4_amax(x.data_ptr(), dt, rows, cols, x.stride(0), seed, _ptr(amax_plain),
                           _ptr(amax_rht), _ptr(workspace), workspace.numel(), _stream(stream)),
            "nvfp4_amax")
+
+
+def nvfp4_quantize_rowcol(x: torch.Tensor, row_flags: int = 0, col_flags: int = 0, seed: int = 0,
+                          row_offset: int = 0, col_offset: int = 0,
+                          row_out: QTensor | None = None, col_out: QTensor | None = None,
+                          amax_row: torch.Tensor | None = None, amax_col: torch.Tensor | None = None,
+                          stream=None):
+    """Row-wise and column-wise quantisation of a bf16 x from one read (see
+    nvfp4_quantize_rowcol in nvfp4.h).  The two amaxes are given: either
+    already in row_out.amax / col_out.amax, or as 1-element float32 CUDA
+    tensors amax_row / amax_col (copied there).  Returns (row_out, col_out)."""
+    if x.dim() != 2 or x.stride(1) != 1 or x.dtype != torch.bfloat16:
+        raise ValueError("x must be a 2-D bf16 tensor with unit column stride")
+    rows, cols = x.shape
+    row_flags |= AMAX_GIVEN
+    col_flags |= AMAX_GIVEN
+    if row_out is None:
+        row_out = alloc_qtensor(rows, cols, ROW_1X16, device=x.device)
+    if col_out is None:
+        col_out = alloc_qtensor(rows, cols, COL_1X16, device=x.device)
+    if amax_row is not None:
+        row_out.amax.copy_(amax_row.reshape(1))
+    if amax_col is not None:
+        col_out.amax.copy_(amax_col.reshape(1))
+    _check(lib.nvfp4_quantize_rowcol(x.data_ptr(), IN_BF16, rows, cols, x.stride(0), row_flags,
+                                     col_flags, seed, row_offset, col_offset, C.byref(row_out.desc),
+                                     C.byref(col_out.desc), _stream(stream)),
+           "nvfp4_quantize_rowcol")
+    return row_out, col_out
 
 
 def nvfp4_quantize_noalloc(x: torch.Tensor, mode: int, flags: int = 0, seed: int = 0,
@@ -375,6 +409,59 @@ def nvfp4_mlp_bwd(p: MlpParams, dY, saved, dX, dWg, dWu, dWd, workspace, stream=
                              dWg.data_ptr(), dWu.data_ptr(), dWd.data_ptr(), workspace.data_ptr(),
                              workspace.numel(), _stream(stream)), "nvfp4_mlp_bwd")
     return dX
+
+
+# intermediates of an MLP step inside the saved / workspace buffers
+MLP_G, MLP_U, MLP_H, MLP_DH, MLP_DG, MLP_DU, MLP_DX_GATE = range(7)
+(MLP_Q_WG, MLP_Q_WU, MLP_Q_WD, MLP_Q_X, MLP_Q_XC, MLP_Q_H, MLP_Q_HC, MLP_Q_DY, MLP_Q_DYC,
+ MLP_Q_DG, MLP_Q_DGC, MLP_Q_DU, MLP_Q_DUC) = range(16, 29)
+
+
+def _slice_of(ptr, nbytes, bufs):
+    """The bytes [ptr, ptr + nbytes) as a uint8 view of whichever buffer holds them."""
+    for b in bufs:
+        if b is not None and b.data_ptr() <= ptr and ptr + nbytes <= b.data_ptr() + b.numel():
+            off = ptr - b.data_ptr()
+            return b[off:off + nbytes]
+    raise ValueError("address outside the given buffers")
+
+
+def mlp_tensor(M, D, F, saved, workspace, which) -> torch.Tensor:
+    """The bf16 intermediate `which` (MLP_G ... MLP_DX_GATE) of the last MLP
+    call, as a [rows, cols] view into saved / workspace (nvfp4_mlp_tensor)."""
+    p, r, c = C.c_void_p(), C.c_int64(), C.c_int64()
+    _check(lib.nvfp4_mlp_tensor(M, D, F, _ptr(saved), _ptr(workspace), which, C.byref(p),
+                                C.byref(r), C.byref(c)), "nvfp4_mlp_tensor")
+    raw = _slice_of(p.value, r.value * c.value * 2, (saved, workspace))
+    return raw.view(torch.bfloat16).view(r.value, c.value)
+
+
+def mlp_operand(M, D, F, saved, workspace, which) -> QTensor:
+    """The quantised operand `which` (MLP_Q_*) of the last MLP call, as a
+    QTensor whose tensors are views into saved / workspace (nvfp4_mlp_operand)."""
+    d = Tensor()
+    _check(lib.nvfp4_mlp_operand(M, D, F, _ptr(saved), _ptr(workspace), which, C.byref(d)),
+           "nvfp4_mlp_operand")
+    bufs = (saved, workspace)
+    rows, cols = d.rows, d.cols
+    # the operand's sizes: K-major [rows, cols] (the quantiser's ROW_1X16 form of the same shape)
+    cb, sb, _, _ = quantize_sizes(rows, cols, ROW_1X16)
+    q = QTensor(codes=_slice_of(d.codes, cb, bufs), scales=_slice_of(d.scales, sb, bufs),
+                amax=_slice_of(d.amax, 4, bufs).view(torch.float32),
+                s_dec=_slice_of(d.s_dec, 4, bufs).view(torch.float32), desc=d)
+    if d.codes_t:
+        cbt, sbt, _, _ = quantize_sizes(cols, rows, ROW_1X16)
+        q.codes_t = _slice_of(d.codes_t, cbt, bufs)
+        q.scales_t = _slice_of(d.scales_t, sbt, bufs)
+    return q
+
+
+STALL_QUANTIZE, STALL_GEMM = 1, 2
+
+
+def debug_inject(stall_mask: int = 0, wait_limit_ns: int = 0):
+    """Failure injection for tests of the bounded waits (nvfp4_debug_inject)."""
+    _check(lib.nvfp4_debug_inject(stall_mask, wait_limit_ns), "nvfp4_debug_inject")
 
 
 def check_device_errors(stream=None):

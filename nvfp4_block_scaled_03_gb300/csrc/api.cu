@@ -71,6 +71,16 @@ nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream) {
   return (gcode || qcode) ? NVFP4_ERR_DEVICE_TIMEOUT : NVFP4_OK;
 }
 
+nvfp4_status nvfp4_debug_inject(uint32_t stall_mask, uint64_t wait_limit_ns) {
+  if (stall_mask & ~(uint32_t)(NVFP4_STALL_QUANTIZE | NVFP4_STALL_GEMM))
+    return NVFP4_ERR_INVALID_ARG;
+  const unsigned long long ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
+  if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+  nvfp4_status st = quant_set_injection((stall_mask & NVFP4_STALL_QUANTIZE) ? 1u : 0u, ns);
+  if (st != NVFP4_OK) return st;
+  return gemm_set_injection((stall_mask & NVFP4_STALL_GEMM) ? 1u : 0u, ns);
+}
+
 nvfp4_status nvfp4_quantize_sizes(int64_t rows, int64_t cols, int32_t mode, uint32_t flags,
                                   size_t* codes_bytes, size_t* scales_bytes,
                                   size_t* scales_t_bytes, size_t* workspace_bytes) {
@@ -94,6 +104,15 @@ nvfp4_status nvfp4_quantize(const void* x, int32_t in_dtype, int64_t rows, int64
                             size_t workspace_bytes, nvfp4_stream stream) {
   return quantize_impl(x, in_dtype, rows, cols, ld, mode, flags, seed, offset, out, workspace,
                        workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_quantize_rowcol(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                   int64_t ld, uint32_t row_flags, uint32_t col_flags,
+                                   uint64_t seed, uint64_t row_offset, uint64_t col_offset,
+                                   nvfp4_tensor* row_out, nvfp4_tensor* col_out,
+                                   nvfp4_stream stream) {
+  return quantize_rowcol_impl(x, in_dtype, rows, cols, ld, row_flags, col_flags, seed, row_offset,
+                              col_offset, row_out, col_out, static_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_amax(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,

@@ -29,6 +29,11 @@
 namespace nvfp4 {
 
 static __device__ unsigned int g_gemm_error;
+// Failure injection for tests of the bounded waits (nvfp4_debug_inject),
+// single-SM kernel only: while g_gemm_stall is set its producer issues no
+// loads, and its pipeline waits give up after g_gemm_wait_ns.
+static __device__ unsigned int g_gemm_stall;
+static __device__ unsigned long long g_gemm_wait_ns = 2000000000ull;
 
 namespace {
 
@@ -106,10 +111,11 @@ NVFP4_DEV bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_f
                             unsigned int code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = *reinterpret_cast<volatile unsigned long long*>(&g_gemm_wait_ns);
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       atomicCAS(&g_gemm_error, 0u, code);
       return false;
@@ -240,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s = 0, ph = 0;
       int armed[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = -1;
-      bool ok = true;
+      // injected stall: no loads, so the MMA thread's first wait runs out
+      bool ok = *reinterpret_cast<volatile unsigned int*>(&g_gemm_stall) == 0u;
       for (int unit = unit0; ok && unit < num_units; unit += unit_step) {
         const int m_blk = unit % num_mu, n_blk = unit / num_mu;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -914,6 +921,13 @@ EncodeTiledFn tensor_map_encoder() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+nvfp4_status gemm_set_injection(unsigned int stall, unsigned long long wait_ns) {
+  if (cudaMemcpyToSymbol(g_gemm_stall, &stall, sizeof(stall)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_gemm_wait_ns, &wait_ns, sizeof(wait_ns)) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
 }
 
 nvfp4_status gemm_read_error(unsigned int* code) {

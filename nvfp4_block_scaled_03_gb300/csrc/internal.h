@@ -31,6 +31,12 @@ nvfp4_status quantize_impl(const void* x, int32_t in_dtype, int64_t rows, int64_
                            uint64_t offset, nvfp4_tensor* out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
+nvfp4_status quantize_rowcol_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                  int64_t ld, uint32_t row_flags, uint32_t col_flags,
+                                  uint64_t seed, uint64_t row_offset, uint64_t col_offset,
+                                  nvfp4_tensor* row_out, nvfp4_tensor* col_out,
+                                  cudaStream_t stream);
+
 nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor* B,
                        int32_t b_view, void* D, int32_t d_mode, const void* C, int64_t M,
                        int64_t N, int64_t K, int32_t tile, cudaStream_t stream);
@@ -68,6 +74,10 @@ nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t co
 
 // Reads and clears the quantisers' device error word (after a sync).
 nvfp4_status quant_read_error(unsigned int* code);
+
+// Failure injection of nvfp4_debug_inject: stall flag and pipeline wait limit.
+nvfp4_status quant_set_injection(unsigned int stall, unsigned long long wait_ns);
+nvfp4_status gemm_set_injection(unsigned int stall, unsigned long long wait_ns);
 
 nvfp4_status gemm_mx_impl(const void* a_codes, const void* a_sf, const void* b_codes,
                           const void* b_sf, int32_t fmt, void* D, int64_t M, int64_t N,

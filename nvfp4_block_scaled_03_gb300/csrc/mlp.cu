@@ -104,8 +104,8 @@ bool dims_ok(int64_t M, int64_t D, int64_t F) {
 // A bf16 operand [rows, cols] quantised twice -- row-wise (FPROP / DGRAD
 // operand) and column-wise (WGRAD operand).  With amax_given, row->amax and
 // col->amax already hold the tensor amaxes (written by the kernel that
-// produced x); otherwise both are taken from one read of x first.  The two
-// quantise passes then use them as given.
+// produced x); otherwise both are taken from one read of x first.  Both
+// operands then come from one more read of x.
 nvfp4_status quantize_pair(const void* x, int64_t rows, int64_t cols, uint32_t row_flags,
                            uint32_t col_flags, uint64_t seed, uint64_t row_offset,
                            uint64_t col_offset, nvfp4_tensor* row, nvfp4_tensor* col,
@@ -119,11 +119,9 @@ nvfp4_status quantize_pair(const void* x, int64_t rows, int64_t cols, uint32_t r
             cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
-  NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_ROW_1X16,
-                          row_flags | NVFP4_AMAX_GIVEN, seed, row_offset, row, nullptr, 0, st));
-  NVFP4_TRY(quantize_impl(x, NVFP4_IN_BF16, rows, cols, cols, NVFP4_COL_1X16,
-                          col_flags | NVFP4_AMAX_GIVEN, seed, col_offset, col, nullptr, 0, st));
-  return NVFP4_OK;
+  return quantize_rowcol_impl(x, NVFP4_IN_BF16, rows, cols, cols, row_flags | NVFP4_AMAX_GIVEN,
+                              col_flags | NVFP4_AMAX_GIVEN, seed, row_offset, col_offset, row, col,
+                              st);
 }
 
 }  // namespace
@@ -226,6 +224,77 @@ nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void
   // WGRAD of gate and up: dWg += dG^T . X, dWu += dU^T . X
   NVFP4_TRY(gemm_impl(&w.qdGc, 0, &s.qXc, 0, dWg, NVFP4_D_F32_ACCUM, nullptr, F, D, M, 0, st));
   NVFP4_TRY(gemm_impl(&w.qdUc, 0, &s.qXc, 0, dWu, NVFP4_D_F32_ACCUM, nullptr, F, D, M, 0, st));
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_mlp_tensor(int64_t M, int64_t D, int64_t F, const void* saved,
+                              const void* workspace, int32_t which, void** data, int64_t* rows,
+                              int64_t* cols) {
+  if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
+  if (!data || !rows || !cols) return NVFP4_ERR_INVALID_ARG;
+  Saved s;
+  Work w;
+  size_t sb = 0, wb = 0;
+  carve_saved(const_cast<void*>(saved), M, D, F, &s, &sb);
+  carve_work(const_cast<void*>(workspace), M, D, F, &w, &wb);
+  void* p = nullptr;
+  int64_t r = M, c = F;
+  switch (which) {
+    case NVFP4_MLP_G: p = s.G; break;
+    case NVFP4_MLP_U: p = s.U; break;
+    case NVFP4_MLP_H: p = w.H; break;
+    case NVFP4_MLP_DH: p = w.dH; break;
+    case NVFP4_MLP_DG: p = w.dG; break;
+    case NVFP4_MLP_DU: p = w.dU; break;
+    case NVFP4_MLP_DX_GATE: p = w.dXg; c = D; break;
+    default: return NVFP4_ERR_INVALID_ARG;
+  }
+  const bool in_saved = which == NVFP4_MLP_G || which == NVFP4_MLP_U;
+  if (!(in_saved ? saved : workspace)) return NVFP4_ERR_INVALID_ARG;
+  *data = p;
+  *rows = r;
+  *cols = c;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_mlp_operand(int64_t M, int64_t D, int64_t F, const void* saved,
+                               const void* workspace, int32_t which, nvfp4_tensor* out) {
+  if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
+  if (!out) return NVFP4_ERR_INVALID_ARG;
+  Saved s;
+  Work w;
+  size_t sb = 0, wb = 0;
+  carve_saved(const_cast<void*>(saved), M, D, F, &s, &sb);
+  carve_work(const_cast<void*>(workspace), M, D, F, &w, &wb);
+  const nvfp4_tensor* t = nullptr;
+  int64_t r = 0, c = 0;  // the operand's logical (K-major) shape
+  bool in_saved = true;
+  switch (which) {
+    case NVFP4_MLP_Q_WG: t = &s.qWg; r = F; c = D; break;
+    case NVFP4_MLP_Q_WU: t = &s.qWu; r = F; c = D; break;
+    case NVFP4_MLP_Q_WD: t = &s.qWd; r = D; c = F; break;
+    case NVFP4_MLP_Q_XC: t = &s.qXc; r = D; c = M; break;
+    case NVFP4_MLP_Q_HC: t = &s.qHc; r = F; c = M; break;
+    default: in_saved = false; break;
+  }
+  if (!in_saved) {
+    switch (which) {
+      case NVFP4_MLP_Q_X: t = &w.qX; r = M; c = D; break;
+      case NVFP4_MLP_Q_H: t = &w.qH; r = M; c = F; break;
+      case NVFP4_MLP_Q_DY: t = &w.qdY; r = M; c = D; break;
+      case NVFP4_MLP_Q_DYC: t = &w.qdYc; r = D; c = M; break;
+      case NVFP4_MLP_Q_DG: t = &w.qdG; r = M; c = F; break;
+      case NVFP4_MLP_Q_DGC: t = &w.qdGc; r = F; c = M; break;
+      case NVFP4_MLP_Q_DU: t = &w.qdU; r = M; c = F; break;
+      case NVFP4_MLP_Q_DUC: t = &w.qdUc; r = F; c = M; break;
+      default: return NVFP4_ERR_INVALID_ARG;
+    }
+  }
+  if (!(in_saved ? saved : workspace)) return NVFP4_ERR_INVALID_ARG;
+  *out = *t;
+  out->rows = r;
+  out->cols = c;
+  out->flags = t->codes_t ? (uint32_t)NVFP4_EMIT_T : 0u;
   return NVFP4_OK;
 }
 

@@ -26,6 +26,11 @@
 namespace nvfp4 {
 
 static __device__ unsigned int g_quant_error;
+// Failure injection for tests of the bounded waits (nvfp4_debug_inject):
+// while g_q_stall is set the quantise passes' producers issue no loads, so
+// the consumers' waits run out; pipeline waits give up after g_q_wait_ns.
+static __device__ unsigned int g_q_stall;
+static __device__ unsigned long long g_q_wait_ns = 2000000000ull;
 
 namespace {
 
@@ -133,10 +138,11 @@ NVFP4_DEV float2 lds2(const uint8_t* st, int r, int c, const float*) {
 NVFP4_DEV bool q_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = *reinterpret_cast<volatile unsigned long long*>(&g_q_wait_ns);
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kQWaitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       atomicCAS(&g_quant_error, 0u, code);
       return false;
@@ -285,6 +291,7 @@ NVFP4_DEV void q_produce(const CUtensorMap* tm, uint32_t stage0, uint32_t bar_fu
                          int64_t ntc) {
   prefetch_tmap(tm);
   int64_t k = 0;
+  if (*reinterpret_cast<volatile unsigned int*>(&g_q_stall)) return;  // injected: no loads
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_empty + 8 * s, (uint32_t)((k / G::kStages) & 1) ^ 1u, abort_flag, 0x40u))
@@ -384,7 +391,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 template <bool RHT, bool SR>
 NVFP4_DEV void col_block(float (&v)[16], int ol, int j, bool rows_ok, int64_t c0, int64_t r0,
                          int64_t R, int64_t C, float s_enc, const float* tab, uint32_t sign_bits,
-                         const QParams& p, uint32_t* out_s, uint8_t* atom) {
+                         const PhiloxKeys& rk, uint64_t offset, uint32_t* out_s, uint8_t* atom) {
   const int64_t col = c0 + ol;
   const bool ok = rows_ok && col < C;
   if (RHT) rht16_block(v, sign_bits);
@@ -398,7 +405,7 @@ NVFP4_DEV void col_block(float (&v)[16], int ol, int j, bool rows_ok, int64_t c0
   if (SR && ok) {
     const uint64_t idx = (uint64_t)(col * R + r0 + 16 * j);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = sr_words(p.rk, p.offset, idx + 4 * q);
+    for (int q = 0; q < 4; ++q) w[q] = sr_words(rk, offset, idx + 4 * q);
   }
   float lo[8], hi[8];
 #pragma unroll
@@ -469,9 +476,10 @@ __global__ void __launch_bounds__(kQThreads, 2)
     uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
     uint8_t* atom = smem + L::offExtra + buf * kBuf + kOutBytes;
     const bool rows_ok = r0 + 16 * j < R;
-    col_block<RHT, SR>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p, out_s, atom);
-    col_block<RHT, SR>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p, out_s,
-                       atom);
+    col_block<RHT, SR>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p.rk, p.offset,
+                       out_s, atom);
+    col_block<RHT, SR>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p.rk,
+                       p.offset, out_s, atom);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_out + 8 * buf);
     if (!q_wait(bar_out + 8 * buf, (uint32_t)((k >> 1) & 1), abort_flag, 0x42u)) break;
@@ -491,6 +499,170 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
     if (warp == 0)
       reinterpret_cast<uint4*>(p.scales + (tc * apr + tr) * 512)[lane] =
+          reinterpret_cast<const uint4*>(atom)[lane];
+  }
+}
+
+// =============================================================================
+// ROW_1X16 and COL_1X16 from one read (the two quantisations a training step
+// makes of an activation or a gradient: the FPROP / DGRAD operand and the
+// WGRAD operand), bf16 input, both tensor amaxes given.  Tile = 64 input rows
+// x 128 input columns, read once from the stage by two sets of lanes:
+//   column role (as quant_col_kernel): lane = column pair, warp pair = 16-row
+//     block -> one output atom of the transposed operand, staged and stored
+//     as coalesced rows after the out barrier;
+//   row role: thread t owns input row t / 4 and the two 16-element blocks at
+//     columns 32 (t % 4) .. + 31 -> 16 bytes of row codes and two scale bytes
+//     (one 16-bit word of the row operand's scale atom), stored directly.
+// The row operand's tiles are half an atom high; the tile that ends the last
+// atom's first half also writes the zero scale rows of its second half.
+// =============================================================================
+struct QRowColParams {
+  int64_t rows, cols;
+  uint64_t seed, row_offset, col_offset;
+  uint8_t* row_codes;
+  uint8_t* row_scales;
+  uint8_t* col_codes;
+  uint8_t* col_scales;
+  float* row_s_dec;
+  float* col_s_dec;
+  const float* row_amax;
+  const float* col_amax;
+  int row_codes_vec16;  // row codes 16-byte aligned rows (else 8)
+  int col_codes_vec16;
+  PhiloxKeys rk;
+};
+using RowColL = QSmem<ColGeo<uint16_t>, 2 * kColBuf + 512>;  // + the row operand's encode table
+
+template <bool RHT, bool SRR, bool SRC>
+__global__ void __launch_bounds__(kQThreads, 2)
+    quant_rowcol_kernel(const __grid_constant__ CUtensorMap tm, const QRowColParams p) {
+  using G = ColGeo<uint16_t>;
+  using L = RowColL;
+  constexpr int kOutWords = kColOutWords;
+  constexpr uint32_t kOutBytes = kColOutBytes, kBuf = kColBuf;
+  extern __shared__ uint8_t q_smem_raw[];
+  uint8_t* smem = align_smem_1024(q_smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar_full = smem_u32(smem + L::offBar);
+  const uint32_t bar_empty = bar_full + 8 * G::kStages;
+  const uint32_t bar_out = bar_full + 16 * G::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
+  float* tab_c = reinterpret_cast<float*>(smem + L::offTab);
+  float* tab_r = reinterpret_cast<float*>(smem + L::offExtra + 2 * kBuf);
+  q_init<G, L>(smem);
+  const float s_enc_r = per_tensor_s_enc(*p.row_amax), s_enc_c = per_tensor_s_enc(*p.col_amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.row_s_dec = __fdiv_rn(1.0f, s_enc_r);
+    *p.col_s_dec = __fdiv_rn(1.0f, s_enc_c);
+  }
+  fill_enc_table(tab_r, s_enc_r);
+  fill_enc_table(tab_c, s_enc_c);
+
+  const int64_t R = p.rows, C = p.cols;
+  const int64_t ntc = (C + G::kTC - 1) / G::kTC, ntr = (R + G::kTR - 1) / G::kTR;
+  const int64_t ntiles = ntr * ntc;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) q_produce<G>(&tm, smem_u32(smem), bar_full, bar_empty, abort_flag, ntiles, ntc);
+    return;
+  }
+  const int cp = lane + 32 * (warp & 1), j = warp >> 1;  // column role
+  const int rr = tid >> 2, bp = tid & 3;                   // row role
+  const int64_t apr_c = ((R / 16) + 3) / 4;  // atoms per 128 rows of the column operand
+  const int64_t pc4_r = ((C / 16) + 3) / 4 * 4;  // padded scale columns of the row operand
+  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % G::kStages);
+    if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
+    const uint8_t* st = smem + s * G::kStageBytes;
+    float va[16], vb[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float2 f = lds2<G>(st, 16 * j + e, 2 * cp, static_cast<const uint16_t*>(nullptr));
+      va[e] = f.x;
+      vb[e] = f.y;
+    }
+
+    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
+    // ---- column operand: staged for the coalesced stores below
+    const int buf = (int)(k & 1);
+    uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
+    uint8_t* atom = smem + L::offExtra + buf * kBuf + kOutBytes;
+    const bool rows_ok = r0 + 16 * j < R;
+    col_block<RHT, SRC>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, sign_bits, p.rk,
+                        p.col_offset, out_s, atom);
+    col_block<RHT, SRC>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, sign_bits, p.rk,
+                        p.col_offset, out_s, atom);
+    // ---- row operand: row r, columns cb .. cb + 31 (two blocks); its values
+    // are read from the stage after the column role's, then the stage is freed
+    {
+      float vr[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        lds8<G>(st, rr, 32 * bp + 8 * q, static_cast<const uint16_t*>(nullptr), vr[q]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      const int64_t r = r0 + rr, cb = c0 + 32 * bp;
+      const bool row_ok = r < R;
+      uint32_t words[4], scw = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const bool ok = row_ok && cb + 16 * b < C;
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fmaxf(fabsf(vr[2 * b][e]), fabsf(vr[2 * b + 1][e])));
+        const uint32_t sc = ok ? block_scale_code(m, s_enc_r) : 0u;
+        const float enc = encode_factor(tab_r, sc);
+        uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0, w2 = w0, w3 = w0;
+        if (SRR && ok) {
+          const uint64_t idx = (uint64_t)(r * C + cb + 16 * b);
+          w0 = sr_words(p.rk, p.row_offset, idx);
+          w1 = sr_words(p.rk, p.row_offset, idx + 4);
+          w2 = sr_words(p.rk, p.row_offset, idx + 8);
+          w3 = sr_words(p.rk, p.row_offset, idx + 12);
+        }
+        words[2 * b] = encode8<SRR>(vr[2 * b], enc, w0, w1);
+        words[2 * b + 1] = encode8<SRR>(vr[2 * b + 1], enc, w2, w3);
+        scw |= sc << (8 * b);
+      }
+      if (row_ok && cb < C) {
+        uint8_t* dst = p.row_codes + r * (C / 2) + cb / 2;
+        if (cb + 32 <= C && p.row_codes_vec16) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+        } else {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+          if (cb + 16 < C) *reinterpret_cast<uint2*>(dst + 8) = make_uint2(words[2], words[3]);
+        }
+      }
+      // scale bytes of scale columns cb/16, cb/16 + 1 (within one 4-byte group:
+      // cb/16 is even); columns past C are zero padding
+      if (cb / 16 < pc4_r)
+        *reinterpret_cast<uint16_t*>(p.row_scales + sf_offset(r, cb / 16, pc4_r)) = (uint16_t)scw;
+      // the second half of the last atom's rows, if no tile covers it: zeros
+      if (tr == ntr - 1 && (r0 & 127) == 0 && cb / 16 < pc4_r)
+        *reinterpret_cast<uint16_t*>(p.row_scales + sf_offset(r + 64, cb / 16, pc4_r)) = 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_out + 8 * buf);
+    if (!q_wait(bar_out + 8 * buf, (uint32_t)((k >> 1) & 1), abort_flag, 0x42u)) break;
+    // column operand rows 16 w .. 16 w + 15: lane -> row 16 w + lane / 2, words 4 (lane % 2) ..
+    const int orl = 16 * warp + (lane >> 1), wq = (lane & 1) * 4;
+    const int64_t orow = c0 + orl;
+    if (orow < C) {
+      uint8_t* dst = p.col_codes + orow * (R / 2) + r0 / 2 + wq * 4;
+      const uint32_t* src = out_s + orl * kOutWords + wq;
+      if (p.col_codes_vec16 && r0 + 8 * (wq + 4) <= R) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (r0 + 8 * (wq + q) < R) reinterpret_cast<uint32_t*>(dst)[q] = src[q];
+      }
+    }
+    if (warp == 0)
+      reinterpret_cast<uint4*>(p.col_scales + (tc * apr_c + tr) * 512)[lane] =
           reinterpret_cast<const uint4*>(atom)[lane];
   }
 }
@@ -902,7 +1074,88 @@ nvfp4_status launch_quant(const QParams& p, int mode, int sms, cudaStream_t s) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+template <auto KERN>
+nvfp4_status launch_rowcol(const CUtensorMap& tm, const QRowColParams& p, int64_t ntiles, int sms,
+                           cudaStream_t s) {
+  static LaunchState ls;
+  const int per_sm = resident_per_sm(ls, KERN, kQThreads, RowColL::kAlloc);
+  if (per_sm <= 0) return NVFP4_ERR_CUDA;
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
+  KERN<<<grid, kQThreads, RowColL::kAlloc, s>>>(tm, p);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 }  // namespace
+
+nvfp4_status quantize_rowcol_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                  int64_t ld, uint32_t row_flags, uint32_t col_flags,
+                                  uint64_t seed, uint64_t row_offset, uint64_t col_offset,
+                                  nvfp4_tensor* row_out, nvfp4_tensor* col_out,
+                                  cudaStream_t stream) {
+  if (!x || !row_out || !col_out) return NVFP4_ERR_INVALID_ARG;
+  for (const nvfp4_tensor* t : {row_out, col_out})
+    if (!t->codes || !t->scales || !t->amax || !t->s_dec) return NVFP4_ERR_INVALID_ARG;
+  if (in_dtype != NVFP4_IN_BF16) return NVFP4_ERR_INVALID_ARG;
+  if ((row_flags & ~(uint32_t)(NVFP4_SR | NVFP4_AMAX_GIVEN)) ||
+      (col_flags & ~(uint32_t)(NVFP4_SR | NVFP4_RHT | NVFP4_AMAX_GIVEN)) ||
+      !(row_flags & NVFP4_AMAX_GIVEN) || !(col_flags & NVFP4_AMAX_GIVEN))
+    return NVFP4_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || rows % 16 || cols % 16) return NVFP4_ERR_SHAPE;
+  if (rows > INT32_MAX || cols > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (!aligned16(x) || (ld * 2) % 16) return NVFP4_ERR_ALIGN;
+  for (const nvfp4_tensor* t : {row_out, col_out})
+    if (!aligned16(t->codes) || !aligned16(t->scales) ||
+        (reinterpret_cast<uintptr_t>(t->amax) & 3u) || (reinterpret_cast<uintptr_t>(t->s_dec) & 3u))
+      return NVFP4_ERR_ALIGN;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+
+  QRowColParams p;
+  p.rows = rows;
+  p.cols = cols;
+  p.seed = seed;
+  p.row_offset = row_offset;
+  p.col_offset = col_offset;
+  p.row_codes = static_cast<uint8_t*>(row_out->codes);
+  p.row_scales = static_cast<uint8_t*>(row_out->scales);
+  p.col_codes = static_cast<uint8_t*>(col_out->codes);
+  p.col_scales = static_cast<uint8_t*>(col_out->scales);
+  p.row_s_dec = row_out->s_dec;
+  p.col_s_dec = col_out->s_dec;
+  p.row_amax = row_out->amax;
+  p.col_amax = col_out->amax;
+  p.row_codes_vec16 = (cols / 2) % 16 == 0;
+  p.col_codes_vec16 = (rows / 2) % 16 == 0;
+  p.rk = philox_round_keys(seed);
+  using G = ColGeo<uint16_t>;
+  CUtensorMap tm;
+  if (!make_input_map<uint16_t>(&tm, x, rows, cols, ld, G::kTR)) return NVFP4_ERR_CUDA;
+  const int64_t nt = ((rows + G::kTR - 1) / G::kTR) * ((cols + G::kTC - 1) / G::kTC);
+  const bool rht = col_flags & NVFP4_RHT, srr = row_flags & NVFP4_SR, src = col_flags & NVFP4_SR;
+  const int sms = dev.sm_count;
+  if (rht) {
+    if (srr && src) st = launch_rowcol<quant_rowcol_kernel<true, true, true>>(tm, p, nt, sms, stream);
+    else if (srr) st = launch_rowcol<quant_rowcol_kernel<true, true, false>>(tm, p, nt, sms, stream);
+    else if (src) st = launch_rowcol<quant_rowcol_kernel<true, false, true>>(tm, p, nt, sms, stream);
+    else st = launch_rowcol<quant_rowcol_kernel<true, false, false>>(tm, p, nt, sms, stream);
+  } else {
+    if (srr && src) st = launch_rowcol<quant_rowcol_kernel<false, true, true>>(tm, p, nt, sms, stream);
+    else if (srr) st = launch_rowcol<quant_rowcol_kernel<false, true, false>>(tm, p, nt, sms, stream);
+    else if (src) st = launch_rowcol<quant_rowcol_kernel<false, false, true>>(tm, p, nt, sms, stream);
+    else st = launch_rowcol<quant_rowcol_kernel<false, false, false>>(tm, p, nt, sms, stream);
+  }
+  if (st != NVFP4_OK) return st;
+  row_out->rows = rows;
+  row_out->cols = cols;
+  row_out->mode = NVFP4_ROW_1X16;
+  row_out->flags = row_flags;
+  col_out->rows = cols;
+  col_out->cols = rows;
+  col_out->mode = NVFP4_COL_1X16;
+  col_out->flags = col_flags;
+  return NVFP4_OK;
+}
 
 // One read of x for the amax of its row-wise and column-wise (RHT) quantisations.
 nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t cols, int64_t ld,
@@ -956,6 +1209,13 @@ nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t co
   float* out1 = amax_rht ? amax_plain : nullptr;
   amax_finalize_kernel<<<1, kAmaxThreads, 0, stream>>>(p.partials, grid, out0, out1);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status quant_set_injection(unsigned int stall, unsigned long long wait_ns) {
+  if (cudaMemcpyToSymbol(g_q_stall, &stall, sizeof(stall)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_q_wait_ns, &wait_ns, sizeof(wait_ns)) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
 }
 
 nvfp4_status quant_read_error(unsigned int* code) {

@@ -49,13 +49,15 @@ def mlp_fwd(X, Wg, Wu, Wd, seed: int = 0, rht: bool = True):
     qH = quantize(H, ROW_1X16)
     qHc = quantize(H, COL_1X16, rf, seed=seed)
     Y = _bf16_gemm(qH, qWd)
-    saved = {"G": G, "U": U, "H": H, "qXc": qXc, "qHc": qHc, "qWg": qWg, "qWu": qWu,
-             "qWd": qWd, "seed": seed, "rht": rht}
+    saved = {"G": G, "U": U, "H": H, "qX": qX, "qXc": qXc, "qH": qH, "qHc": qHc, "qWg": qWg,
+             "qWu": qWu, "qWd": qWd, "seed": seed, "rht": rht}
     return Y, saved
 
 
 def mlp_bwd(dY, saved, dWg, dWu, dWd, step: int = 0):
-    """dY bf16 bits [M, D]; dWg, dWu, dWd float32 master gradients, updated in place."""
+    """dY bf16 bits [M, D]; dWg, dWu, dWd float32 master gradients, updated in place.
+    Returns dX and the backward's intermediates (dH, dG, dU as bf16 bits and
+    the six quantised gradient operands)."""
     seed, rf = saved["seed"], (RHT if saved["rht"] else 0)
     off = sr_offsets(step)
     qdY = quantize(dY, ROW_1X16, SR, seed=seed, offset=off["dy_row"])
@@ -71,4 +73,5 @@ def mlp_bwd(dY, saved, dWg, dWu, dWd, step: int = 0):
                         gemm_fp64(qdU, transposed_view(saved["qWu"])))
     dWg += bf16_to_f32(_bf16_gemm(qdGc, saved["qXc"]))
     dWu += bf16_to_f32(_bf16_gemm(qdUc, saved["qXc"]))
-    return dX, {"dH": dH, "dG": dG, "dU": dU}
+    return dX, {"dH": dH, "dG": dG, "dU": dU, "qdY": qdY, "qdYc": qdYc, "qdG": qdG,
+                "qdGc": qdGc, "qdU": qdU, "qdUc": qdUc}

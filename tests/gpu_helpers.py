@@ -78,3 +78,73 @@ def assert_gemm_close(got: np.ndarray, ref: np.ndarray, name: str = "", rms=None
     assert not bad.any(), (f"{name}: {int(bad.sum())} elements beyond 4 ulp + 1e-3 rms; worst "
                            f"err {err[bad].max():.3e} at ref {ref[bad][np.argmax(err[bad])]:.3e}")
     return rel
+
+
+# ---- sampled comparisons at sizes the oracle cannot take whole -------------
+# An operand row of a 1x16 or 16x16 quantisation depends only on its own input
+# row (ROW_1X16, BLOCK_16X16) or input column (COL_1X16), the tensor amax and,
+# for stochastic rounding, its own Philox counters: the oracle quantises
+# 128-row slabs of the operand with the tensor amax given and each element's
+# SR index taken in the whole operand (sr_index_base), and those slabs must
+# equal the GPU's bytes.  The GEMM is then checked on sampled outputs whose
+# rows and columns lie in the checked slabs.
+def oracle_slabs(orc, x, mode, flags, amax, slabs, seed=0, offset=0):
+    """Oracle quantisation of 128-row slabs `slabs` of the operand that
+    quantising x [R, C] (bf16 bits or float32) in `mode` gives."""
+    R, Cn = x.shape
+    _, ocols = orc.out_shape(mode, R, Cn)
+    out = []
+    for sl in slabs:
+        r0 = sl * 128
+        xs = np.ascontiguousarray(x[:, r0:r0 + 128] if mode == orc.COL_1X16 else x[r0:r0 + 128])
+        out.append(orc.quantize(xs, mode, flags, seed=seed, offset=offset,
+                                amax_given=float(amax), sr_index_base=r0 * ocols))
+    return out
+
+
+def oracle_slabs_transposed(orc, w, amax, slabs):
+    """Slabs of the transposed view of a 16x16 weight quantisation of w [R, C]:
+    operand rows c0 .. c0 + 127 are input columns, quantised from w[:, c0:]."""
+    out = []
+    for sl in slabs:
+        ws = np.ascontiguousarray(w[:, sl * 128:sl * 128 + 128])
+        o = orc.quantize(ws, orc.BLOCK_16X16, orc.EMIT_T, amax_given=float(amax))
+        out.append({"codes": o["codes_t"], "scales": o["scales_t"], "scales_sw": o["scales_t_sw"],
+                    "s_dec": o["s_dec"], "rows": 128, "cols": o["rows"]})
+    return out
+
+
+def assert_slabs_equal(codes, scales_sw, amax, s_dec, oslabs, slabs, name):
+    """GPU operand (codes [rows, cols/2] uint8, MMA-layout scales, amax, s_dec
+    as numpy) against oracle slabs, bit for bit."""
+    ocols = codes.shape[1] * 2
+    atom_bytes = ((ocols // 16 + 3) // 4) * 512
+    for sl, o in zip(slabs, oslabs):
+        if not np.array_equal(codes[sl * 128:sl * 128 + 128], o["codes"]):
+            bad = np.argwhere(codes[sl * 128:sl * 128 + 128] != o["codes"])
+            raise AssertionError(f"{name}: slab {sl}: {len(bad)} code bytes differ, first {bad[:4]}")
+        got = scales_sw[sl * atom_bytes:(sl + 1) * atom_bytes]
+        assert np.array_equal(got, o["scales_sw"]), f"{name}: slab {sl}: scale atoms differ"
+        assert np.float32(o["s_dec"]).view(np.uint32) == np.float32(s_dec).view(np.uint32), name
+        if "amax" in o:
+            assert np.float32(o["amax"]).view(np.uint32) == np.float32(amax).view(np.uint32), name
+
+
+def compact_operand(oslabs):
+    """The oracle slabs as one operand dict of their rows (row-major scales)."""
+    return {"codes": np.ascontiguousarray(np.concatenate([o["codes"] for o in oslabs])),
+            "scales": np.ascontiguousarray(np.concatenate([o["scales"] for o in oslabs])),
+            "s_dec": oslabs[0]["s_dec"], "rows": 128 * len(oslabs), "cols": oslabs[0]["cols"]}
+
+
+def sampled_positions(a_slabs, b_slabs, n=4096, seed=11):
+    """(local m, local n, global m, global n): every output of the first
+    slab pair and of the last slab pair, plus n random outputs over all the
+    slabs' rows and columns."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    na, nb = 128 * len(a_slabs), 128 * len(b_slabs)
+    g0 = np.meshgrid(np.arange(128), np.arange(128), indexing="ij")
+    lm = np.concatenate([g0[0].ravel(), na - 128 + g0[0].ravel(), rng.integers(0, na, n)])
+    ln = np.concatenate([g0[1].ravel(), nb - 128 + g0[1].ravel(), rng.integers(0, nb, n)])
+    to_g = lambda loc, slabs: np.asarray(slabs)[loc // 128] * 128 + loc % 128  # noqa: E731
+    return lm, ln, to_g(lm, a_slabs), to_g(ln, b_slabs)

@@ -141,3 +141,103 @@ def test_swiglu_argument_errors_return_before_any_launch(lib):
     assert bwd(t, t, t, t, t, 32, 64, 0, 0, a, a, a, a, None, wsb, None) == 5
     assert bwd(t, t, t, t, t + 4, 32, 64, 0, 0, a, a, a, a, ws, wsb, None) == 3
     assert bwd(t, t, t, t, t, 32, 64, 0, 0, a, a, a + 2, a, ws, wsb, None) == 3  # amax not 4-aligned
+
+
+class _Desc(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("codes_t", C.c_void_p),
+                ("scales_t", C.c_void_p), ("amax", C.c_void_p), ("s_dec", C.c_void_p),
+                ("rows", C.c_int64), ("cols", C.c_int64), ("mode", C.c_int32),
+                ("flags", C.c_uint32)]
+
+
+def test_mlp_intermediates_lie_inside_their_buffers(lib):
+    """nvfp4_mlp_tensor / nvfp4_mlp_operand are host-side address arithmetic:
+    with stand-in buffer addresses, every intermediate lies inside the buffer
+    the header names for it, 256-byte aligned, with the stated shape, and no
+    two intermediates overlap."""
+    M, D, F = 384, 256, 640
+    sb, wb = C.c_size_t(), C.c_size_t()
+    assert lib.nvfp4_mlp_sizes(C.c_int64(M), C.c_int64(D), C.c_int64(F), C.byref(sb),
+                               C.byref(wb)) == 0
+    saved, ws = 1 << 40, 1 << 44            # stand-ins; nothing is dereferenced
+    lib.nvfp4_mlp_tensor.argtypes = [C.c_int64] * 3 + [C.c_void_p, C.c_void_p, C.c_int32,
+                                                       C.POINTER(C.c_void_p),
+                                                       C.POINTER(C.c_int64), C.POINTER(C.c_int64)]
+    lib.nvfp4_mlp_operand.argtypes = [C.c_int64] * 3 + [C.c_void_p, C.c_void_p, C.c_int32,
+                                                        C.POINTER(_Desc)]
+    spans = []
+
+    def inside(ptr, n, in_saved):
+        base, size = (saved, sb.value) if in_saved else (ws, wb.value)
+        assert base <= ptr and ptr + n <= base + size
+        assert ptr % 256 == 0
+        spans.append((ptr, ptr + n))
+
+    shapes = {0: (M, F), 1: (M, F), 2: (M, F), 3: (M, F), 4: (M, F), 5: (M, F), 6: (M, D)}
+    for which, shape in shapes.items():
+        p, r, c = C.c_void_p(), C.c_int64(), C.c_int64()
+        assert lib.nvfp4_mlp_tensor(M, D, F, saved, ws, which, C.byref(p), C.byref(r),
+                                    C.byref(c)) == 0
+        assert (r.value, c.value) == shape
+        inside(p.value, r.value * c.value * 2, which in (0, 1))
+    ops = {16: (F, D, 1), 17: (F, D, 1), 18: (D, F, 1), 19: (M, D, 0), 20: (D, M, 1),
+           21: (M, F, 0), 22: (F, M, 1), 23: (M, D, 0), 24: (D, M, 0), 25: (M, F, 0),
+           26: (F, M, 0), 27: (M, F, 0), 28: (F, M, 0)}
+    for which, (rows, cols, in_saved) in ops.items():
+        d = _Desc()
+        assert lib.nvfp4_mlp_operand(M, D, F, saved, ws, which, C.byref(d)) == 0
+        assert (d.rows, d.cols) == (rows, cols)
+        pr, pc = (rows + 127) // 128 * 128, (cols // 16 + 3) // 4 * 4
+        inside(d.codes, rows * cols // 2, in_saved)
+        inside(d.scales, pr * pc, in_saved)
+        inside(d.amax, 4, in_saved)
+        inside(d.s_dec, 4, in_saved)
+        if which in (16, 17, 18):
+            inside(d.codes_t, rows * cols // 2, in_saved)
+            inside(d.scales_t, (cols + 127) // 128 * 128 * ((rows // 16 + 3) // 4 * 4), in_saved)
+        else:
+            assert not d.codes_t and not d.scales_t
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:])), "intermediates overlap"
+    d = _Desc()
+    p, r, c = C.c_void_p(), C.c_int64(), C.c_int64()
+    assert lib.nvfp4_mlp_operand(M, D, F, saved, ws, 99, C.byref(d)) == 1      # unknown
+    assert lib.nvfp4_mlp_operand(M, D, F, None, ws, 16, C.byref(d)) == 1       # holder NULL
+    assert lib.nvfp4_mlp_operand(M, D, F, saved, None, 16, C.byref(d)) == 0    # other NULL ok
+    assert lib.nvfp4_mlp_tensor(M, D, F, saved, None, 2, C.byref(p), C.byref(r), C.byref(c)) == 1
+    assert lib.nvfp4_mlp_tensor(100, D, F, saved, ws, 2, C.byref(p), C.byref(r), C.byref(c)) == 2
+
+
+def test_quantize_rowcol_argument_errors_before_any_launch(lib):
+    """nvfp4_quantize_rowcol rejects bad arguments on the host, before any CUDA
+    call: stand-in addresses suffice (nothing is dereferenced)."""
+    f = lib.nvfp4_quantize_rowcol
+    f.argtypes = [C.c_void_p, C.c_int32, C.c_int64, C.c_int64, C.c_int64, C.c_uint32,
+                  C.c_uint32, C.c_uint64, C.c_uint64, C.c_uint64, C.POINTER(_Desc),
+                  C.POINTER(_Desc), C.c_void_p]
+    base = 1 << 40
+
+    def desc(k):
+        d = _Desc()
+        d.codes, d.scales, d.amax, d.s_dec = base + k * 4096, base + k * 4096 + 1024, \
+            base + k * 4096 + 2048, base + k * 4096 + 2052
+        return d
+
+    x, G = base + (1 << 20), 8  # AMAX_GIVEN
+    r, c = desc(1), desc(2)
+
+    def call(x=x, dt=0, rows=64, cols=64, ld=64, rf=G, cf=G | 1, r=r, c=c):
+        return f(x, dt, rows, cols, ld, rf, cf, 0, 0, 0, C.byref(r) if r else None,
+                 C.byref(c) if c else None, None)
+
+    assert call(x=None) == 1                      # NULL input
+    assert call(c=None) == 1                      # NULL output descriptor
+    assert call(dt=1) == 1                        # fp32 input
+    assert call(rf=0) == 1                        # amax not given
+    assert call(rf=G | 1) == 1                    # RHT on the row operand
+    assert call(cf=G | 4) == 1                    # EMIT_T
+    assert call(rows=40) == 2 and call(cols=72, ld=72) == 2 and call(ld=32) == 2
+    assert call(x=x + 8) == 3 and call(ld=68) == 3
+    bad = desc(3)
+    bad.codes += 4
+    assert call(r=bad) == 3                       # codes not 16-byte aligned

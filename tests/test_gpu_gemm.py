@@ -202,3 +202,95 @@ def _check_sampled(nv, orc, name, a, b):
     ref = orc.gemm_fp64_sampled(a, b, m, n)
     H.assert_gemm_close(H.host_f64(D[m, n]), ref, name)
     del A, B, D
+
+
+@pytest.mark.parametrize("M,K,N,tile", [(128, 256, 512, 0), (512, 256, 784, 3)])
+def test_gemm_zero_operand(nv, orc, M, K, N, tile):
+    """An all-zero operand quantises to s_dec = 1, zero scales and zero codes
+    (the zero-amax edge of the per-tensor scale); its product with any
+    operand is exactly zero, on the single-SM and the CTA-pair kernels."""
+    import torch
+    X, W, _ = syn.linear_layer(M, K, N)
+    Z = np.zeros((M, K), np.uint16)
+    qZ = nv.nvfp4_quantize(H.dev_bf16(Z), nv.ROW_1X16)
+    qW = nv.nvfp4_quantize(H.dev_bf16(W), nv.BLOCK_16X16, nv.EMIT_T)
+    oZ = orc.quantize(Z, orc.ROW_1X16)
+    H.assert_quant_equal(qZ, oZ, "zeros")
+    assert float(qZ.s_dec.cpu()[0]) == 1.0 and not qZ.scales.cpu().numpy().any()
+    for D in (nv.nvfp4_gemm(qZ, qW, tile=tile),
+              nv.nvfp4_gemm(qW, qZ, tile=tile if tile == 0 else 2),
+              nv.nvfp4_gemm(qZ, qZ, tile=tile)):
+        nv.check_device_errors()
+        assert not torch.any(D.float() != 0), "a product with a zero operand is not zero"
+    ref = orc.gemm_fp64(oZ, orc.quantize(W, orc.BLOCK_16X16, orc.EMIT_T))
+    assert not ref.any()
+
+
+def test_gemm_405b_down_projection_gpu_quantised_sampled(nv, orc):
+    """The Llama-3.1-405B MLP down projection at full size: H [8192, 53248]
+    (activations), W_down [16384, 53248], dY [8192, 16384]; FPROP Y = H W^T
+    (K = 53248), DGRAD dH = dY W through W's transposed view (K = 16384),
+    WGRAD dW = dY^T H (K = 8192, both RHT, dY^T with SR).  The GPU quantises
+    every operand whole; the oracle takes each tensor's amax itself and
+    quantises sampled 128-row slabs of every operand, which must equal the
+    GPU's bytes, and the GEMMs are checked on the first and last slab pairs'
+    outputs plus 4096 random outputs within the slabs."""
+    import gc
+    import torch
+    M, N, K = 8192, 16384, 53248
+    rng = np.random.Generator(np.random.PCG64(21))
+
+    def pick(n):
+        k = n // 128
+        return sorted({0, k - 1} | set(rng.integers(1, k - 1, 2).tolist()))
+
+    Hh = syn.activations((M, K), seed=1)
+    W = syn.weights((N, K), seed=2)
+    dY = syn.gradients((M, N), seed=3)
+    sM, sN, sK = pick(M), pick(N), pick(K)
+
+    def host_q(q):
+        return (q.codes.cpu().numpy().reshape(q.rows, q.cols // 2), q.scales.cpu().numpy(),
+                float(q.amax.cpu()[0]), float(q.s_dec.cpu()[0]))
+
+    def oracle_op(x, mode, flags, q, slabs, name, offset=0):
+        amax = orc.amax(x, mode, flags & orc.RHT, seed=0)
+        codes, scales, a, sd = host_q(q)
+        assert np.float32(a) == amax, name
+        os_ = H.oracle_slabs(orc, x, mode, flags, amax, slabs, seed=0, offset=offset)
+        H.assert_slabs_equal(codes, scales, a, sd, os_, slabs, name)
+        return H.compact_operand(os_)
+
+    def check(D, a, b, sa, sb, name):
+        nv.check_device_errors()
+        lm, ln, gm, gn = H.sampled_positions(sa, sb)
+        ref = orc.gemm_fp64_sampled(a, b, lm, ln)
+        got = H.host_f64(D[torch.from_numpy(gm).cuda(), torch.from_numpy(gn).cuda()])
+        H.assert_gemm_close(got, ref, name)
+
+    qW = nv.nvfp4_quantize(H.dev_bf16(W), nv.BLOCK_16X16, nv.EMIT_T)
+    wamax = orc.amax(W, orc.BLOCK_16X16)
+    assert np.float32(float(qW.amax.cpu()[0])) == wamax
+    codes, scales, a, sd = host_q(qW)
+    oW = H.oracle_slabs(orc, W, orc.BLOCK_16X16, orc.EMIT_T, wamax, sN)
+    H.assert_slabs_equal(codes, scales, a, sd, oW, sN, "W")
+    codes_t = qW.codes_t.cpu().numpy().reshape(K, N // 2)
+    oWt = H.oracle_slabs_transposed(orc, W, wamax, sK)
+    H.assert_slabs_equal(codes_t, qW.scales_t.cpu().numpy(), a, sd, oWt, sK, "W^T")
+    oW, oWt = H.compact_operand(oW), H.compact_operand(oWt)
+    del W
+    gc.collect()
+    qH = nv.nvfp4_quantize(H.dev_bf16(Hh), nv.ROW_1X16)
+    check(nv.nvfp4_gemm(qH, qW), oracle_op(Hh, orc.ROW_1X16, 0, qH, sM, "H"), oW, sM, sN,
+          "FPROP 405B down")
+    del qH
+    qdY = nv.nvfp4_quantize(H.dev_bf16(dY), nv.ROW_1X16, nv.SR, seed=0, offset=0)
+    check(nv.nvfp4_gemm(qdY, qW, b_view=1),
+          oracle_op(dY, orc.ROW_1X16, orc.SR, qdY, sM, "dY"), oWt, sM, sK, "DGRAD 405B down")
+    del qdY, qW
+    torch.cuda.empty_cache()
+    qdYc = nv.nvfp4_quantize(H.dev_bf16(dY), nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1)
+    qHc = nv.nvfp4_quantize(H.dev_bf16(Hh), nv.COL_1X16, nv.RHT, seed=0)
+    a_op = oracle_op(dY, orc.COL_1X16, orc.RHT | orc.SR, qdYc, sN, "dY^T", offset=1)
+    b_op = oracle_op(Hh, orc.COL_1X16, orc.RHT, qHc, sK, "H^T")
+    check(nv.nvfp4_gemm(qdYc, qHc), a_op, b_op, sN, sK, "WGRAD 405B down")

@@ -118,6 +118,53 @@ def test_mx_gemm_405b_up_projection_sampled(nv, orc, fmt):
     H.assert_gemm_close(got, ref, f"{fmt} 405B up projection")
 
 
+def _mx_dev(nv, t, mode, f):
+    import torch
+    swb = nv.mx_sizes(t.shape[0], t.shape[1], mode, f)[2]
+    sw = torch.empty(swb, dtype=torch.uint8, device="cuda")
+    codes, _ = nv.nvfp4_mx_quantize(H.dev_bf16(t), mode, f, scales_sw=sw)
+    return codes, sw
+
+
+def _mx_rows(orc, x, mode, f, rows):
+    """Dequantised operand rows `rows` of the MX quantisation of x: a row of
+    the row form is an input row, of the column form an input column (MX
+    blocks are local to it: no tensor scale)."""
+    xs = np.ascontiguousarray(x[:, rows] if mode == orc.MX_COL else x[rows])
+    return orc.mx_dequant(orc.mx_quantize(xs, mode, f))
+
+
+@pytest.mark.parametrize("fmt", ["MXFP8", "MXFP4"])
+def test_mx_gemm_405b_dgrad_wgrad_sampled(nv, orc, fmt):
+    """The Llama-3.1-405B up projection's DGRAD (dX = dY W: dY [8192, 53248]
+    row form, W read through its column form, K = 53248) and WGRAD (dW = dY^T X:
+    both column forms, K = 8192) at full size on GPU-quantised operands,
+    checked on 4096 sampled outputs against the oracle's quantisation of the
+    sampled operand rows."""
+    import torch
+    f = {"MXFP4": nv.MXFP4, "MXFP8": nv.MXFP8}[fmt]
+    X, W = _405b_inputs()
+    M, K = X.shape
+    N = W.shape[0]
+    dY = syn.gradients((M, N), seed=3)
+    rng = np.random.default_rng(13)
+    for name, (a, am, b, bm, gm, gn, gk) in {
+            "DGRAD": (dY, orc.MX_ROW, W, orc.MX_COL, M, K, N),
+            "WGRAD": (dY, orc.MX_COL, X, orc.MX_COL, N, K, M)}.items():
+        (ca, sa), (cb, sb) = _mx_dev(nv, a, am, f), _mx_dev(nv, b, bm, f)
+        D = nv.nvfp4_mx_gemm(ca, sa, cb, sb, f, gm, gn, gk)
+        nv.check_device_errors()
+        del ca, sa, cb, sb
+        rows_m = np.unique(rng.integers(0, gm, 256))
+        rows_n = np.unique(rng.integers(0, gn, 256))
+        m, n = rng.choice(rows_m, 4096), rng.choice(rows_n, 4096)
+        da, db = _mx_rows(orc, a, am, f, rows_m), _mx_rows(orc, b, bm, f, rows_n)
+        ref = np.einsum("ij,ij->i", da[np.searchsorted(rows_m, m)], db[np.searchsorted(rows_n, n)])
+        got = H.host_f64(D[torch.from_numpy(m).cuda(), torch.from_numpy(n).cuda()])
+        H.assert_gemm_close(got, ref, f"{fmt} 405B {name}")
+        del D
+
+
 def test_mx_gemm_rejects_bad_arguments(nv):
     import torch
     z = torch.zeros(4096, dtype=torch.uint8, device="cuda")

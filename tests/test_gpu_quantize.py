@@ -200,3 +200,56 @@ def test_amax_rejects_bad_arguments(nv):
     assert e.value.status == nv.ERR_INVALID_ARG
     nv.nvfp4_amax(x, amax_plain=a)                   # the plain amax has no row constraint
     assert float(a.cpu()[0]) == 0.0
+
+
+def _edge_rows(C):
+    """bf16 [64, C] whose 16-element row blocks (and, because the 16 rows of
+    each 16-row strip repeat one pattern, whose 16x16 tiles) reach the rarely
+    taken branches of the quantiser: with the tensor amax given as 2688
+    (s_enc = 1, so a block's scale is E4M3(max/6)) --
+      T        every E2M1 tie (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, signed)
+               under a block maximum of 6 (scale 1, encode factor 1);
+      Z        -0 and negative values that round to zero in a non-zero block;
+      T * 2^-8 a subnormal E4M3 scale (2^-8);
+      T * 2^-9 the smallest subnormal scale (2^-9);
+      T * 2^-10 a scale exactly halfway to zero (rounds to 0: codes 0 / -0);
+      T * 2^-12 a scale far below (0);
+      T * 16   a large normal scale;
+    and a Gaussian strip.  With the amax given as 26.88 (s_enc = 100, below
+    the true maximum) block scales clamp at 448 and elements saturate at 6."""
+    T = np.array([6, .25, .75, 1.25, 1.75, 2.5, 3.5, 5, -.25, -.75, -1.25, -1.75, -2.5, -3.5,
+                  -5, .5], np.float32)
+    Z = np.array([6, -0.0, -0.1, -0.2, -0.24, 0.1, 0.2, -0.0, 0.0, -6, -0.3, 0.3, -0.26, 0.26,
+                  -0.01, -0.0], np.float32)
+    pats = [T, Z, T * 2.0 ** -8, T * 2.0 ** -9, T * 2.0 ** -10, T * 2.0 ** -12, T * 16,
+            Z * 2.0 ** -8]
+    rng = np.random.Generator(np.random.PCG64(17))
+    x = np.empty((64, C), np.float32)
+    for r in range(64):
+        for j in range(C // 16):
+            k = ((r // 16) * (C // 16) + j) % (len(pats) + 1)
+            x[r, 16 * j:16 * j + 16] = (pats[k] if k < len(pats)
+                                        else rng.standard_normal(16).astype(np.float32) * 3)
+    return syn.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("amax", [2688.0, 26.88, None])
+@pytest.mark.parametrize("mode_name,spec", MODES)
+def test_quantize_edge_cases(nv, orc, mode_name, spec, amax):
+    """Ties, signed zeros, subnormal and zero block scales, saturation: codes,
+    scales, amax and s_dec bit for bit against the oracle, in every mode (the
+    column mode reads the transpose, so its 16-row blocks hold the patterns)."""
+    x = _edge_rows(256)
+    if mode_name == "COL":
+        x = np.ascontiguousarray(x.T)
+    mode, flags = _mode(nv, mode_name), _flags(nv, spec)
+    q = nv.nvfp4_quantize(H.dev_bf16(x), mode, flags, seed=9, offset=1, amax=amax)
+    o = orc.quantize(x, _mode(orc, mode_name), _flags(orc, spec), seed=9, offset=1,
+                     amax_given=amax)
+    H.assert_quant_equal(q, o, f"edge {mode_name}/{spec}/amax={amax}")
+    if amax == 2688.0 and not (flags & nv.RHT):
+        codes = q.codes.cpu().numpy()
+        # the patterns reach what they are there for: negative zeros (code 8)
+        # and, in the blocks under a zero scale, all-zero magnitudes
+        assert ((codes & 0xF) == 8).any() or ((codes >> 4) == 8).any()
+        assert (q.scales.cpu().numpy() == 0).any()

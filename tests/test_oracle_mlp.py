@@ -101,3 +101,134 @@ def test_nvfp4_mlp_tracks_fp64_mlp(orc, rht):
     # a swapped operand, a sign error or a row permutation is far outside it
     assert _rel(dWg, rdWu) > 1.0 and _rel(_f64(dX), -rdX) > 1.5
     assert _rel(_f64(Y), rY[::-1]) > 1.0
+
+
+# ---- the recipe's per-operand choices inside the composition -------------------
+_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _sr_decisions(orc, q, v_bits):
+    """For each element of the quantised operand q of the bf16 values v (in
+    q's output layout): frac = (|y| - lo) / (hi - lo) of y = v * s_enc / S_b
+    on the E2M1 grid, and whether the code took hi; elements on the grid or
+    saturated are dropped.  Float64 here: only used to bin fractions."""
+    v = np.abs(syn.bf16_bits_to_f32(v_bits).astype(np.float64))
+    S = np.array([orc.e4m3_value(int(b)) for b in range(256)])[q["scales"]]
+    S = np.repeat(S, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(S > 0, v * float(q["s_enc"]) / S, 0.0)
+    codes = q["codes"]
+    nib = np.empty((codes.shape[0], codes.shape[1] * 2), np.uint8)
+    nib[:, 0::2], nib[:, 1::2] = codes & 7, (codes >> 4) & 7
+    mag = _GRID[nib]
+    hi_i = np.clip(np.searchsorted(_GRID, y, side="right"), 1, 7)
+    lo, hi = _GRID[hi_i - 1], _GRID[hi_i]
+    keep = (y < 6.0) & (y != lo) & (S > 0)
+    frac = (y - lo) / (hi - lo)
+    return frac[keep], (mag == hi)[keep], keep
+
+
+def _rht_of_transpose(x_bits, seed):
+    """(1/4) H16 diag(s) applied to each 16-element block of every row of x^T
+    (x: bf16 bits [M, N] -> [N, M] float64), H16 = scipy's Sylvester matrix."""
+    from scipy.linalg import hadamard
+    import oracle as orc
+    xt = syn.bf16_bits_to_f32(x_bits).astype(np.float64).T
+    T = hadamard(16) @ np.diag(orc.rht_signs(seed).astype(np.float64)) / 4.0
+    n, m = xt.shape
+    return (xt.reshape(n, m // 16, 16) @ T.T).reshape(n, m)
+
+
+@pytest.fixture(scope="module")
+def mlp_run(orc):
+    from oracle.mlp import mlp_bwd, mlp_fwd
+    M, D, F = 256, 64, 128
+    X = syn.activations((M, D), seed=1)
+    Wg = syn.weights((F, D), seed=4, master_fp32=True) * np.float32(5)
+    Wu = syn.weights((F, D), seed=5, master_fp32=True) * np.float32(5)
+    Wd = syn.weights((D, F), seed=6, master_fp32=True) * np.float32(5)
+    dY = syn.gradients((M, D), seed=3)
+    _, saved = mlp_fwd(X, Wg, Wu, Wd, seed=7, rht=True)
+    steps = []
+    for step in (0, 1):
+        dW = [np.zeros_like(w) for w in (Wg, Wu, Wd)]
+        steps.append(mlp_bwd(dY, saved, *dW, step=step)[1])
+    return X, dY, saved, steps
+
+
+def test_mlp_gradient_operands_are_stochastically_rounded(orc, mlp_run):
+    """dY, dG, dU (row and column operands) are stochastically rounded: an
+    element rounds up with probability equal to its fraction between the
+    two grid neighbours (binomial bound per fraction bin), so round-to-
+    nearest -- up exactly when frac > 1/2 -- fails every bin."""
+    X, dY, saved, steps = mlp_run
+    b = steps[0]
+    srcs = {"qdY": dY, "qdG": b["dG"], "qdU": b["dU"]}
+    for name in ("qdY", "qdG", "qdU"):
+        frac, up, _ = _sr_decisions(orc, b[name], srcs[name])
+        for lo_f, hi_f in ((0.05, 0.2), (0.2, 0.4), (0.6, 0.8), (0.8, 0.95)):
+            sel = (frac >= lo_f) & (frac < hi_f)
+            n = int(sel.sum())
+            assert n > 500, (name, lo_f, n)
+            p, want = up[sel].mean(), frac[sel].mean()
+            assert abs(p - want) < 5 * np.sqrt(0.25 / n), (name, lo_f, p, want)
+
+
+def test_mlp_sr_operands_draw_independent_words(orc, mlp_run):
+    """The six SR operands of a step, and one operand across two steps, draw
+    their Philox words independently (distinct counter offsets): the rounding
+    decisions of any two, paired by output index, are uncorrelated.  Sharing
+    an offset would pair identical words, r < T1 and r < T2, a correlation of
+    (min(f1, f2) - f1 f2) / sqrt(f1 (1 - f1) f2 (1 - f2)), about 0.5 here."""
+    X, dY, saved, steps = mlp_run
+    from oracle.mlp import sr_offsets
+    assert len(set(sr_offsets(0).values()) | set(sr_offsets(1).values())) == 12
+    b0, b1 = steps
+
+    def dec(b, name, src):
+        q = b[name]
+        if name.endswith("c"):
+            return None   # column operands: their fractions need the transformed values
+        frac, up, keep = _sr_decisions(orc, q, src)
+        f = np.full(keep.shape, np.nan)
+        u = np.full(keep.shape, np.nan)
+        f[keep], u[keep] = frac, up
+        return f.ravel(), u.ravel()
+
+    ops = {("0", "qdY"): dec(b0, "qdY", dY), ("0", "qdG"): dec(b0, "qdG", b0["dG"]),
+           ("0", "qdU"): dec(b0, "qdU", b0["dU"]), ("1", "qdG"): dec(b1, "qdG", b1["dG"])}
+    keys = list(ops)
+    for i in range(len(keys)):
+        for j in range(i + 1, len(keys)):
+            (f1, u1), (f2, u2) = ops[keys[i]], ops[keys[j]]
+            n = min(len(f1), len(f2))
+            f1, u1, f2, u2 = f1[:n], u1[:n], f2[:n], u2[:n]
+            ok = ~(np.isnan(f1) | np.isnan(f2))
+            num = np.sum((u1[ok] - f1[ok]) * (u2[ok] - f2[ok]))
+            den = np.sqrt(np.sum(f1[ok] * (1 - f1[ok])) * np.sum(f2[ok] * (1 - f2[ok])))
+            c = num / den
+            assert abs(c) < 5 / np.sqrt(ok.sum()), (keys[i], keys[j], c)
+    # the column operands: same words would make their codes' parity pattern
+    # repeat the row operand's at equal linear index; check code agreement is
+    # at the level two independent roundings give
+    for name in ("qdYc", "qdGc", "qdUc"):
+        assert not np.array_equal(b0[name]["codes"], b1[name]["codes"]), name
+
+
+def test_mlp_wgrad_operands_carry_the_rht(orc, mlp_run):
+    """Every column (WGRAD) operand of the composition -- X^T, H^T, dY^T, dG^T,
+    dU^T -- encodes (1/4) H16 diag(s) of its tensor's 16-token blocks, with
+    the same signs s for all of them (so the transform cancels in each
+    product): its dequantisation is within NVFP4 noise of that transform
+    (computed here with scipy's Hadamard matrix) and far from the
+    untransformed transpose."""
+    X, dY, saved, steps = mlp_run
+    b = steps[0]
+    for name, q, src in (("X^T", saved["qXc"], X), ("H^T", saved["qHc"], saved["H"]),
+                         ("dY^T", b["qdYc"], dY), ("dG^T", b["qdGc"], b["dG"]),
+                         ("dU^T", b["qdUc"], b["dU"])):
+        deq = orc.dequant(q)
+        T = _rht_of_transpose(src, 7)
+        plain = syn.bf16_bits_to_f32(src).astype(np.float64).T
+        assert _rel(deq, T) < 0.3, (name, _rel(deq, T))
+        assert _rel(deq, plain) > 0.7, (name, _rel(deq, plain))
