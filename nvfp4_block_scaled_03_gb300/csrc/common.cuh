@@ -200,7 +200,9 @@ NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
   const uint32_t code_hi = ge1 ? (t >> 22) - 252u : (t >> 23) - 125u;
   const uint32_t thr = __float2uint_rz(__fmul_rn(__uint_as_float(a), 8589934592.0f));
   uint32_t code = a < 0x3F000000u ? (thr > r ? 1u : 0u) : code_hi;
-  code = a < 0x40C00000u ? code : 7u;  // |y| >= 6 (or not finite) saturates
+  // |y| >= 6 (or not finite) saturates: code_hi is at least 7 there, and never
+  // above 7 below it (lo = 4 rounds up to code 7 at most)
+  code = min(code, 7u);
   return sign | code;
 }
 

@@ -442,16 +442,18 @@ NVFP4_DEV void tc_mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, u
   }
 }
 
-template <int STAGES, int FMT = kFmtNVF4>
+template <int STAGES, int FMT, bool IMG>
 struct PairSmem {
   static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
-  // B's scales as 4 KB images, one per scale atom along K (the two row
-  // halves' atoms, each repeated for the four 32-lane quarters), that one
-  // 128-lane x 256-bit copy each moves into tensor memory
+  // B's scales either as the plain atoms of the tile's two 128-row blocks
+  // (two 32x128b.warpx4 copies per K step), or as 4 KB images, one per scale
+  // atom along K (the two row halves' atoms, each repeated for the four
+  // 32-lane quarters), that one 128-lane x 256-bit copy each moves into
+  // tensor memory
   static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
-  static constexpr uint32_t kSFB = kAt * 4096;                 // the tile's B scale images
+  static constexpr uint32_t kSFB = IMG ? kAt * 4096 : kAt * 1024;
   static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
@@ -489,14 +491,14 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
   }
 }
 
-template <int STAGES, int DMODE, int FMT>
+template <int STAGES, int DMODE, int FMT, bool IMG>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
                           const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
-  using L = PairSmem<STAGES, FMT>;
+  using L = PairSmem<STAGES, FMT, IMG>;
   constexpr int kAt = PairFmt<FMT>::kAtoms;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -568,7 +570,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           // scale atoms as 128-byte rows (4 per atom)
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
                            (a_rb * args.kg + kb * kAt) * 4);
-          tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
+          if (IMG) {
+            tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
+          } else {  // the two row blocks' atoms (a block past N reads as zeros)
+            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, 0,
+                             (b_rb0 * args.kg + kb * kAt) * 4);
+            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + kAt * 512, &tmSFB, fb, 0,
+                             ((b_rb0 + 1) * args.kg + kb * kAt) * 4);
+          }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -602,11 +611,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           for (int j = 0; j < natoms; ++j) {
             if (j % kPairCopyWarps == cw)
               tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
-            if ((kAt + j) % kPairCopyWarps == cw)
-              tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
+            if ((kAt + j) % kPairCopyWarps == cw) {
+              if (IMG) {
+                tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
+              } else {
+                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j, smem_desc_sf(sb + j * 512));
+                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc_sf(sb + (kAt + j) * 512));
+              }
+            }
           }
           issued = true;
-          tc_commit_pair(sf_bar(s), 1);  // the leader's barrier
+          // the MMA thread may issue as soon as these copies are issued: the
+          // fence before this arrive and the MMA thread's fence after its wait
+          // order its MMAs behind them in the tensor pipe
+          tc_fence_before();
+          mbar_arrive(sf_bar(s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -629,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          // the copy warps observed the stage's data, then their copies completed
+          // the copy warps observed the stage's data and issued its scale copies
           if (!wait_bounded_pair(sf_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
             ok = false;
             break;
@@ -825,12 +844,12 @@ bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int STAGES, int DMODE, int FMT = kFmtNVF4>
+template <int STAGES, int DMODE, int FMT, bool IMG>
 nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
                          const CUtensorMap& msb, const CUtensorMap& md, const GemmArgs& a, int sms,
                          cudaStream_t stream) {
-  using L = PairSmem<STAGES, FMT>;
-  auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE, FMT>;
+  using L = PairSmem<STAGES, FMT, IMG>;
+  auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE, FMT, IMG>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
@@ -898,10 +917,14 @@ nvfp4_status launch_pair_mode(int d_mode, const CUtensorMap& ma, const CUtensorM
                               const CUtensorMap& msa, const CUtensorMap& msb,
                               const CUtensorMap& md, const GemmArgs& a, int sms, cudaStream_t s) {
   switch (d_mode) {
-    case NVFP4_D_BF16: return launch_pair<STAGES, NVFP4_D_BF16>(ma, mb, msa, msb, md, a, sms, s);
+    case NVFP4_D_BF16:
+      return launch_pair<STAGES, NVFP4_D_BF16, kFmtNVF4, false>(ma, mb, msa, msb, md, a, sms, s);
     case NVFP4_D_F32_ACCUM:
-      return launch_pair<STAGES, NVFP4_D_F32_ACCUM>(ma, mb, msa, msb, md, a, sms, s);
-    default: return launch_pair<STAGES, NVFP4_D_BF16_ADD_C>(ma, mb, msa, msb, md, a, sms, s);
+      return launch_pair<STAGES, NVFP4_D_F32_ACCUM, kFmtNVF4, false>(ma, mb, msa, msb, md, a, sms,
+                                                                     s);
+    default:
+      return launch_pair<STAGES, NVFP4_D_BF16_ADD_C, kFmtNVF4, false>(ma, mb, msa, msb, md, a, sms,
+                                                                      s);
   }
 }
 
@@ -993,7 +1016,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     CUtensorMap msa, msb, md;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
         !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
-        !make_sf_image_map(&msb, b_sf, a.kg, a.nrb_b, PairFmt<kFmtNVF4>::kAtoms))
+        !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
       return NVFP4_ERR_CUDA;
     // bf16 output map for the tensor-store epilogue (other modes do not use it)
     if (d_mode == NVFP4_D_BF16) {
@@ -1003,7 +1026,7 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
     }
     a.num_m_blk = (int)((M + 255) / 256);
     a.num_n_blk = (int)((N + 255) / 256);
-    return launch_pair_mode<4>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
+    return launch_pair_mode<5>(d_mode, ma, mb, msa, msb, md, a, dev.sm_count, stream);
   }
   const int bn = tile == NVFP4_TILE_128X128 ? 128 : 256;
   const int bkb = tile == NVFP4_TILE_128X256_K128 ? 64 : 128;  // stage K bytes per row
@@ -1053,8 +1076,10 @@ nvfp4_status gemm_mx_impl(const void* a_codes, const void* a_sf, const void* b_c
       !make_out_map(&md, D, M, N))
     return NVFP4_ERR_CUDA;
   return fmt == NVFP4_MXFP4
-             ? launch_pair<5, NVFP4_D_BF16, kFmtMXF4>(ma, mb, msa, msb, md, a, dev.sm_count, stream)
-             : launch_pair<5, NVFP4_D_BF16, kFmtMXF8>(ma, mb, msa, msb, md, a, dev.sm_count, stream);
+             ? launch_pair<5, NVFP4_D_BF16, kFmtMXF4, true>(ma, mb, msa, msb, md, a, dev.sm_count,
+                                                            stream)
+             : launch_pair<5, NVFP4_D_BF16, kFmtMXF8, true>(ma, mb, msa, msb, md, a, dev.sm_count,
+                                                            stream);
 }
 
 }  // namespace nvfp4

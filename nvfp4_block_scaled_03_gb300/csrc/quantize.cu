@@ -242,7 +242,7 @@ NVFP4_DEV uint32_t encode8(const float (&v)[8], float enc, uint4 w0, uint4 w1) {
   if (SR) {
     const uint32_t r[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out |= e2m1_sr(y[i], r[i]) << (4 * i);
+    for (int i = 0; i < 8; ++i) out += e2m1_sr(y[i], r[i]) * (1u << (4 * i));  // disjoint nibbles
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) out |= e2m1x2_rn(y[2 * i], y[2 * i + 1]) << (8 * i);

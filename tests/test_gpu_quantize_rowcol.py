@@ -35,7 +35,7 @@ def _same(a, b, name):
     for f in ("codes", "scales", "amax", "s_dec"):
         ga, gb = getattr(a, f), getattr(b, f)
         assert ga.numel() == gb.numel() and bool((ga == gb).all()), f"{name}: {f} differ"
-    assert (a.rows, a.cols, a.mode) == (b.rows, b.cols, b.mode), name
+    assert (a.rows, a.cols, a.desc.mode) == (b.rows, b.cols, b.desc.mode), name
 
 
 def _run(nv, x, rs, cs, seed=5, ro=2, co=3):
