@@ -37,9 +37,9 @@ METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roof
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM at
 # M=8192, N=14336, K=4096, from one ncu capture of that launch
-# (dram__bytes_read.sum 52.6 MB + dram__bytes_write.sum 188.2 MB); None once
+# (dram__bytes_read.sum 55.5 MB + dram__bytes_write.sum 187.9 MB); None once
 # the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = 52.615424e6 + 188.206080e6  # dram read + write, one FPROP launch
+FPROP_TRAFFIC_BYTES = 55.467776e6 + 187.944448e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
@@ -59,13 +59,18 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="layer",
                    choices=["layer", "mlp", "rht_study", "quant_sweep", "gemm_405b",
-                            "format_study"],
+                            "format_study", "kernel"],
                    help="layer: the linear layer's step (default, the headline); mlp: the "
                         "SwiGLU MLP forward + backward, 9 GEMMs, at --mlp-tokens x 4096 x 14336; "
                         "rht_study: WGRAD error with and without the RHT; quant_sweep: quantiser "
                         "GB/s over four shapes and six forms; gemm_405b: the Llama-3.1-405B MLP "
                         "projections' GEMMs; format_study: NVFP4 against MXFP4 and MXFP8 on the "
-                        "405B up projection's operands")
+                        "405B up projection's operands; kernel: one launch of one kernel "
+                        "family (--kernel) on [8192, 14336], for one-kernel profiler captures")
+    p.add_argument("--kernel", default="rowcol_sr",
+                   choices=["amax", "rowcol_rne", "rowcol_sr", "row_rne", "row_sr", "col_rht_rne",
+                            "col_rht_sr", "w16x16", "mx_row", "mx_col", "gemm_fprop"],
+                   help="--workload kernel: which kernel family to launch")
     p.add_argument("--mlp-tokens", type=int, default=32768)
     return p.parse_args()
 
@@ -972,6 +977,51 @@ def run_format_study(args):
         "result": results, "impl": "ours"}), flush=True)
 
 
+def run_kernel(args):
+    """One launch of one library kernel family on the gradient / activation
+    shape [8192, 14336] (235 MB of bf16, larger than the 129 MB L2), after the
+    one-read amax pass it needs; the weight quantiser on W [14336, 4096]; the
+    GEMM on the FPROP shape.  For one-kernel profiler captures (ncu -k ... -c 1);
+    prints a short JSON line, no timing."""
+    import torch
+
+    from nvfp4_block_scaled_03_gb300 import synthetic as syn
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_block_scaled_03_gb300 import binding as nv
+    form = args.kernel
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+
+    if form == "gemm_fprop":
+        a = nv.nvfp4_quantize(dev(syn.activations((8192, 4096), seed=1)), nv.ROW_1X16)
+        b = nv.nvfp4_quantize(dev(syn.weights((14336, 4096), seed=2)), nv.BLOCK_16X16, nv.EMIT_T)
+        torch.cuda.synchronize()
+        nv.nvfp4_gemm(a, b)
+    elif form == "w16x16":
+        nv.nvfp4_quantize(dev(syn.weights((14336, 4096), seed=2)), nv.BLOCK_16X16, nv.EMIT_T)
+    else:
+        sr = "sr" in form
+        x = dev(syn.gradients((8192, 14336), seed=3) if sr else syn.activations((8192, 14336), seed=1))
+        pa = torch.zeros(1, dtype=torch.float32, device="cuda")
+        ra = torch.zeros(1, dtype=torch.float32, device="cuda")
+        nv.nvfp4_amax(x, pa, ra, seed=0)
+        f = nv.SR if sr else 0
+        if form.startswith("rowcol"):
+            nv.nvfp4_quantize_rowcol(x, f, nv.RHT | f, seed=0, amax_row=pa, amax_col=ra)
+        elif form.startswith("row_"):
+            nv.nvfp4_quantize(x, nv.ROW_1X16, f, amax=pa)
+        elif form.startswith("col_"):
+            nv.nvfp4_quantize(x, nv.COL_1X16, nv.RHT | f, amax=ra)
+        elif form.startswith("mx_"):
+            nv.nvfp4_mx_quantize(x, nv.MX_ROW if form == "mx_row" else nv.MX_COL, nv.MXFP4)
+    torch.cuda.synchronize()
+    nv.check_device_errors()
+    print(json.dumps({"workload": "kernel", "kernel": form, "ok": True}), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3 and args.impl == "ours":
@@ -988,6 +1038,8 @@ def main():
         run_gemm_405b(args)
     elif args.workload == "format_study":
         run_format_study(args)
+    elif args.workload == "kernel":
+        run_kernel(args)
     else:
         run_ours(args)
 

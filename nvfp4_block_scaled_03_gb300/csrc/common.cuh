@@ -194,7 +194,7 @@ NVFP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
 NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
   const uint32_t bits = __float_as_uint(y);
   const uint32_t sign = (bits >> 28) & 8u;
-  const uint32_t a = bits & 0x7FFFFFFFu;
+  const uint32_t a = __float_as_uint(fabsf(y));
   const bool ge1 = a >= 0x3F800000u;
   const uint32_t t = a + ((~r) >> (ge1 ? 10 : 9));
   const uint32_t code_hi = ge1 ? (t >> 22) - 252u : (t >> 23) - 125u;
