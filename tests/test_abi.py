@@ -241,3 +241,11 @@ def test_quantize_rowcol_argument_errors_before_any_launch(lib):
     bad = desc(3)
     bad.codes += 4
     assert call(r=bad) == 3                       # codes not 16-byte aligned
+
+
+def test_debug_inject_rejects_unknown_bits_without_a_device(lib):
+    """nvfp4_debug_inject refuses stall bits it does not know before touching
+    the device."""
+    lib.nvfp4_debug_inject.argtypes = [C.c_uint32, C.c_uint64]
+    assert lib.nvfp4_debug_inject(4, 0) == 1
+    assert lib.nvfp4_debug_inject(0xFFFFFFFC, 1000) == 1
