@@ -378,17 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bytes of the single-CTA 128 x 256 tile and reads half the B operand bytes
 // from its own shared memory per MMA.
 //
-// A single thread pays a fixed issue latency per tcgen05 instruction (tens of
-// cycles), so one thread issuing a stage's 12 scale copies and 4 MMAs cannot
-// keep the tensor pipe busy.  The leader therefore splits the issue: the copy
-// warps each wait for the stage's data, issue their share of its 12 scale
-// copies into both CTAs' tensor memory and commit to the stage's scales-ready
-// barrier;
-// the MMA thread waits for that barrier and issues only the MMAs and the
-// commit that frees the stage.  A tensor-memory scale slot is rewritten only
-// after its stage was refilled, i.e. after the MMAs that read it completed.
-// Each CTA's epilogue drains its 128 accumulator rows and releases them on
-// the leader's barrier.
+// A single thread pays an issue latency of about a hundred cycles per tcgen05
+// instruction, so one thread issuing a stage's 12 scale copies and 4 MMAs
+// cannot keep the tensor pipe busy.  The leader therefore splits the issue:
+// the copy warps each wait for the stage's data, issue their share of its 12
+// scale copies into both CTAs' tensor memory, then fence
+// (tcgen05.fence::before_thread_sync) and arrive on the stage's scales-ready
+// barrier; the MMA thread waits for that barrier, fences
+// (tcgen05.fence::after_thread_sync), which orders its MMAs behind those
+// copies in the tensor pipe without waiting for them to complete, and issues
+// only the MMAs and the commit that frees the stage.  A tensor-memory scale
+// slot is rewritten only after its stage was refilled, i.e. after the MMAs
+// that read it completed.  Each CTA's epilogue drains its 128 accumulator rows
+// and releases them on the leader's barrier.  NVFP4 B scales arrive as the
+// plain atoms of the tile's two 128-row blocks (38 KB a stage, 5 stages); the
+// MX formats, with fewer atoms per stage, take them as replicated images.
 // =============================================================================
 constexpr int kPairBN = 256;
 

@@ -730,7 +730,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
       float m = 0.0f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[b][e]));
-      m = warp_max(m);
+      // the 16x16 block's maximum in one warp reduction: non-negative floats
+      // order like their bit patterns read as unsigned integers
+      m = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
       const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
       const float enc = encode_factor(tab, sc);
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;

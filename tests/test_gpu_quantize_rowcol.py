@@ -90,3 +90,25 @@ def test_rowcol_rejects_bad_arguments(nv):
     with pytest.raises(nv.NVFP4Error) as e:
         nv.nvfp4_quantize_rowcol(x, nv.RHT, 0, row_out=r, col_out=c)   # RHT on the row operand
     assert e.value.status == nv.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("rs,cs", [("", "RHT"), ("SR", "RHT|SR")])
+def test_rowcol_strided_input(nv, orc, rs, cs):
+    """x is a column slice of a wider tensor (leading dimension 208 > 144
+    columns): both operands equal the oracle's quantisation of the slice."""
+    import torch
+    wide = syn.activations((96, 208), seed=4)
+    x = np.ascontiguousarray(wide[:, 32:176])
+    xt = H.dev_bf16(wide)[:, 32:176]
+    assert xt.stride(0) == 208
+    rf, cf = _flags(nv, rs), _flags(nv, cs)
+    a_plain = torch.zeros(1, dtype=torch.float32, device="cuda")
+    a_col = torch.zeros(1, dtype=torch.float32, device="cuda")
+    nv.nvfp4_amax(xt, a_plain, a_col, seed=5)
+    row, col = nv.nvfp4_quantize_rowcol(xt, rf, cf, seed=5, row_offset=2, col_offset=3,
+                                        amax_row=a_plain, amax_col=a_col)
+    nv.check_device_errors()
+    H.assert_quant_equal(row, orc.quantize(x, orc.ROW_1X16, _flags(orc, rs), seed=5, offset=2),
+                         "row strided")
+    H.assert_quant_equal(col, orc.quantize(x, orc.COL_1X16, _flags(orc, cs), seed=5, offset=3),
+                         "col strided")
