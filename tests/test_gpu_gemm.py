@@ -45,7 +45,7 @@ def _gemms(orc, L):
 
 @pytest.mark.parametrize("tile", [1, 2, 3, 5])
 @pytest.mark.parametrize("M,K,N", [(128, 256, 512), (208, 192, 144), (320, 1024, 272),
-                                   (128, 64, 16)])
+                                   (128, 64, 16), (320, 576, 1040)])
 def test_gemm_small(nv, orc, M, K, N, tile):
     L = _layer(orc, M, K, N)
     for name, (a, b) in _gemms(orc, L).items():
@@ -99,7 +99,7 @@ def test_gemm_output_modes(nv, orc):
     nv.check_device_errors()
 
 
-@pytest.mark.parametrize("M,K,N", [(512, 256, 784), (768, 512, 512)])
+@pytest.mark.parametrize("M,K,N", [(512, 256, 784), (768, 512, 512), (512, 320, 1168)])
 def test_gemm_output_modes_pair_kernel(nv, orc, M, K, N):
     """The fold into FP32 and the bf16 add on the CTA-pair kernel (the large-
     shape path), with a ragged last tile: F32_ACCUM equals W0 + float(D)
