@@ -56,6 +56,7 @@ def parse():
     p.add_argument("--k", type=int, default=4096)
     p.add_argument("--n", type=int, default=14336)
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-warmup", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="layer",
                    choices=["layer", "mlp", "rht_study", "quant_sweep", "gemm_405b",
@@ -366,7 +367,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for i in range(args.e2e_steps):
+    for i in range(-args.e2e_warmup, args.e2e_steps):
+        if i == 0:  # the warm-up iterations (untimed) have run
+            torch.cuda.synchronize()
+            barrier()
+            t0 = time.perf_counter()
         b = i % 2
         d = layer.sets[b]
         with torch.cuda.stream(s_in):
@@ -432,7 +437,7 @@ def run_ours(args):
                              "per quantisation (five)"},
         "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "warmup": args.e2e_warmup,
                 "host_link_gbs": link,
                 "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3)},
         "gpu_launches": layer.launches_per_step * args.steps,
@@ -571,6 +576,49 @@ def run_mlp(args):
     torch.cuda.synchronize()
     nv.check_device_errors()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), device) / args.steps
+
+    # A training step: forward + backward + the optimizer step of the three
+    # FP32 masters (SGD, gradients cleared).  Fused: each update writes its
+    # weight's amax into the next forward's operand slot, and the forward
+    # quantises the weights without amax passes.  Unfused: the update alone,
+    # the forward takes the amaxes itself.
+    lr = 1e-6
+    slots = [nv.mlp_operand(M, D, F, saved, ws, w).amax
+             for w in (nv.MLP_Q_WG, nv.MLP_Q_WU, nv.MLP_Q_WD)]
+    sgd_ws = torch.empty(4096, dtype=torch.uint8, device=device)
+
+    def train(i, fused):
+        p = nv.mlp_params(M, D, F, Wg, Wu, Wd, seed=0, step=i, rht=True, weight_amax_given=fused)
+        nv.nvfp4_mlp_fwd(p, X, Y, saved, ws)
+        nv.nvfp4_mlp_bwd(p, dY, saved, dX, gWg, gWu, gWd, ws)
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        for w, g, a in zip((Wg, Wu, Wd), (gWg, gWu, gWd), slots):
+            nv.nvfp4_sgd_step(w, g, lr, zero_grad=True, amax=a if fused else None,
+                              workspace=sgd_ws)
+        return e
+
+    train_ms = {}
+    for fused in (True, False):
+        for i in range(args.warmup):  # the first fused step's amaxes come from warm-up
+            flush.fill_(1)
+            flush_rd.amax()
+            train(i, fused)
+        tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        opt = []
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            flush_rd.amax()
+            tev[i][0].record()
+            opt.append(train(args.warmup + i, fused))
+            tev[i][1].record()
+        torch.cuda.synchronize()
+        nv.check_device_errors()
+        train_ms[fused] = (
+            max_over_ranks(sum(a.elapsed_time(b) for a, b in tev), device) / args.steps,
+            sum(o.elapsed_time(b) for o, (_, b) in zip(opt, tev)) / args.steps)
     flops = 9 * 2.0 * M * D * F
     if rank == 0:
         print(json.dumps({
@@ -582,6 +630,14 @@ def run_mlp(args):
             "config": {"workload": f"SwiGLU MLP fwd+bwd, tokens {M}, hidden {D}, ffn {F}, "
                                    "FP32 master weights and grads",
                        "l2": "flushed before every timed step (256 MiB write + read, untimed)"},
+            "training_step": {
+                "note": "forward + backward + SGD on the three FP32 masters (gradients "
+                        "cleared); fused: the update writes each weight's amax into the next "
+                        "forward's operand slot and the forward skips its three amax passes",
+                "fused_ms": round(train_ms[True][0], 4),
+                "unfused_ms": round(train_ms[False][0], 4),
+                "optimizer_ms_fused": round(train_ms[True][1], 4),
+                "optimizer_ms_unfused": round(train_ms[False][1], 4)},
             "impl": "ours"}), flush=True)
 
 
