@@ -350,7 +350,14 @@ nvfp4_status nvfp4_gemm_ex(const nvfp4_tensor* A, int32_t a_view, const nvfp4_te
  * with RNE (1x16 / 16x16), dY, dG, dU with SR; the WGRAD operands (X^T, H^T,
  * dY^T, dG^T, dU^T) COL_1X16 with the RHT when flags has NVFP4_RHT.
  * Dimensions: M tokens, D hidden, F ffn; Wg, Wu fp32 [F, D], Wd fp32 [D, F]
- * (device, the FP32 master weights, quantised 16x16 every forward). */
+ * (device, the FP32 master weights, quantised 16x16 every forward).
+ * flags: NVFP4_RHT, and NVFP4_AMAX_GIVEN for a forward whose weight amaxes
+ * are already in the weight operands' amax slots in `saved`
+ * (nvfp4_mlp_operand: Q_WG / Q_WU / Q_WD, .amax), e.g. written there by the
+ * previous optimizer step (nvfp4_sgd_step): the three weights are then
+ * quantised without their amax passes, with codes and scales identical to a
+ * forward that takes the amaxes itself.  The backward ignores
+ * NVFP4_AMAX_GIVEN. */
 typedef struct nvfp4_mlp_params {
   int64_t M, D, F;
   const float* Wg;
@@ -358,7 +365,7 @@ typedef struct nvfp4_mlp_params {
   const float* Wd;
   uint64_t seed;   /* RHT signs and SR key                           */
   uint64_t step;   /* SR counter offsets 8*step + 0..5 (per tensor)  */
-  uint32_t flags;  /* NVFP4_RHT or 0                                 */
+  uint32_t flags;  /* NVFP4_RHT | NVFP4_AMAX_GIVEN, or 0             */
 } nvfp4_mlp_params;
 
 /* SwiGLU between the gate/up and down projections, with the tensor amaxes of
@@ -451,6 +458,39 @@ enum {
 };
 nvfp4_status nvfp4_mlp_operand(int64_t M, int64_t D, int64_t F, const void* saved,
                                const void* workspace, int32_t which, nvfp4_tensor* out);
+
+/* ---------------------------------------------------------------------- */
+/* Optimizer step of an FP32 master weight                                  */
+/* ---------------------------------------------------------------------- */
+/* "NVFP4 pretraining recipe" page, Figure 1 text: the MLP GEMMs' BF16
+ * outputs are folded into FP32 master weights on the optimizer step, and
+ * each step quantises the weights 16x16 under a per-tensor FP32 scale taken
+ * from the tensor's amax.  This call is that step for one weight, fused with
+ * the amax of the updated weight, so the next quantisation needs no amax
+ * pass.  The pages name no optimizer: plain SGD on the FP32 master weight W
+ * and the FP32 master gradient G (the WGRAD results the GEMM's
+ * NVFP4_D_F32_ACCUM mode or nvfp4_mlp_bwd folded into it), elementwise in
+ * binary32, the product rounded first:
+ *   W[i]  = W[i] - lr * G[i]
+ *   G[i]  = 0                  with NVFP4_ZERO_GRAD in flags
+ *   *amax = max_i |W[i]|       of the updated W, when amax is not NULL: bit
+ *                              for bit what nvfp4_amax returns for W, so it
+ *                              can be given to the 16x16 quantiser
+ *                              (NVFP4_AMAX_GIVEN), or written straight into
+ *                              an MLP weight operand's amax slot for an
+ *                              nvfp4_mlp_fwd with NVFP4_AMAX_GIVEN.
+ * W, G: device float [n], 16-byte aligned, not overlapping; n > 0, n % 4 == 0;
+ * lr finite.  amax: device float, 4-byte aligned, or NULL.  workspace:
+ * device scratch of at least the nvfp4_quantize_sizes workspace size
+ * (16-byte aligned) when amax is not NULL, else unused (may be NULL);
+ * contents on return unspecified.  One read of W and G, one write of W (and
+ * of G with NVFP4_ZERO_GRAD); two kernel launches on `stream` (one without
+ * amax); nothing is allocated.  Returns NVFP4_ERR_INVALID_ARG (NULL W or G,
+ * W and G overlapping, unknown flag bits, lr not finite), _SHAPE, _ALIGN,
+ * _WORKSPACE, _ARCH, _CUDA. */
+enum { NVFP4_ZERO_GRAD = 16u };
+nvfp4_status nvfp4_sgd_step(float* W, float* G, int64_t n, float lr, uint32_t flags, float* amax,
+                            void* workspace, size_t workspace_bytes, nvfp4_stream stream);
 
 #ifdef __cplusplus
 }

@@ -86,6 +86,7 @@ def _load():
         "nvfp4_mlp_bwd": ([P(MlpParams), vp, vp, vp, vp, vp, vp, vp, sz, vp], C.c_int),
         "nvfp4_mlp_tensor": ([i64, i64, i64, vp, vp, i32, P(vp), P(i64), P(i64)], C.c_int),
         "nvfp4_mlp_operand": ([i64, i64, i64, vp, vp, i32, P(Tensor)], C.c_int),
+        "nvfp4_sgd_step": ([vp, vp, i64, C.c_float, u32, vp, vp, sz, vp], C.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -392,9 +393,10 @@ def mlp_sizes(M, D, F):
     return s.value, w.value
 
 
-def mlp_params(M, D, F, Wg, Wu, Wd, seed=0, step=0, rht=True) -> MlpParams:
+def mlp_params(M, D, F, Wg, Wu, Wd, seed=0, step=0, rht=True,
+               weight_amax_given=False) -> MlpParams:
     return MlpParams(M, D, F, Wg.data_ptr(), Wu.data_ptr(), Wd.data_ptr(), seed, step,
-                     RHT if rht else 0)
+                     (RHT if rht else 0) | (AMAX_GIVEN if weight_amax_given else 0))
 
 
 def nvfp4_mlp_fwd(p: MlpParams, X, Y, saved, workspace, stream=None):
@@ -454,6 +456,31 @@ def mlp_operand(M, D, F, saved, workspace, which) -> QTensor:
         q.codes_t = _slice_of(d.codes_t, cbt, bufs)
         q.scales_t = _slice_of(d.scales_t, sbt, bufs)
     return q
+
+
+ZERO_GRAD = 16
+
+
+def nvfp4_sgd_step(W: torch.Tensor, G: torch.Tensor, lr: float, zero_grad: bool = False,
+                   amax: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None):
+    """W -= lr * G on FP32 master weight and gradient (G zeroed with
+    zero_grad), writing max |W| of the updated weight into the 1-element
+    float32 CUDA tensor `amax` when given (see nvfp4_sgd_step in nvfp4.h)."""
+    for t in (W, G):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("W and G must be contiguous float32 CUDA tensors")
+    if W.numel() != G.numel():
+        raise ValueError("W and G must have the same number of elements")
+    if amax is not None and (amax.dtype != torch.float32 or amax.numel() != 1 or not amax.is_cuda):
+        raise ValueError("amax must be a 1-element float32 CUDA tensor")
+    if amax is not None and workspace is None:
+        workspace = _workspace(quantize_sizes(128, 128, ROW_1X16)[3], W.device)
+    _check(lib.nvfp4_sgd_step(W.data_ptr(), G.data_ptr(), W.numel(), float(lr),
+                              ZERO_GRAD if zero_grad else 0, _ptr(amax), _ptr(workspace),
+                              workspace.numel() if workspace is not None else 0,
+                              _stream(stream)), "nvfp4_sgd_step")
+    return W
 
 
 STALL_QUANTIZE, STALL_GEMM = 1, 2

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libnvfp4.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "swiglu.cu", "mlp.cu", "mx.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "swiglu.cu", "mlp.cu", "mx.cu", "optim.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -149,7 +149,7 @@ nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, vo
                            nvfp4_stream stream) {
   if (!p || !X || !Y || !saved || !workspace || !p->Wg || !p->Wu || !p->Wd)
     return NVFP4_ERR_INVALID_ARG;
-  if (p->flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  if (p->flags & ~(uint32_t)(NVFP4_RHT | NVFP4_AMAX_GIVEN)) return NVFP4_ERR_INVALID_ARG;
   const int64_t M = p->M, D = p->D, F = p->F;
   if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
   Saved s;
@@ -163,12 +163,15 @@ nvfp4_status nvfp4_mlp_fwd(const nvfp4_mlp_params* p, const void* X, void* Y, vo
   void* ws = w.partials;
   const size_t wsb = kQuantWorkspaceBytes;
 
-  NVFP4_TRY(quantize_impl(p->Wg, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
-                          &s.qWg, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(p->Wu, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
-                          &s.qWu, ws, wsb, st));
-  NVFP4_TRY(quantize_impl(p->Wd, NVFP4_IN_FP32, D, F, F, NVFP4_BLOCK_16X16, NVFP4_EMIT_T, 0, 0,
-                          &s.qWd, ws, wsb, st));
+  // the weights' amaxes either taken here or already in their operand slots
+  // (the optimizer step's fused amax, nvfp4_sgd_step)
+  const uint32_t wf = NVFP4_EMIT_T | (p->flags & NVFP4_AMAX_GIVEN);
+  NVFP4_TRY(quantize_impl(p->Wg, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, wf, 0, 0, &s.qWg, ws,
+                          wsb, st));
+  NVFP4_TRY(quantize_impl(p->Wu, NVFP4_IN_FP32, F, D, D, NVFP4_BLOCK_16X16, wf, 0, 0, &s.qWu, ws,
+                          wsb, st));
+  NVFP4_TRY(quantize_impl(p->Wd, NVFP4_IN_FP32, D, F, F, NVFP4_BLOCK_16X16, wf, 0, 0, &s.qWd, ws,
+                          wsb, st));
   NVFP4_TRY(quantize_pair(X, M, D, 0, rht, p->seed, 0, 0, &w.qX, &s.qXc, false, ws, wsb, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWg, 0, s.G, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
   NVFP4_TRY(gemm_impl(&w.qX, 0, &s.qWu, 0, s.U, NVFP4_D_BF16, nullptr, M, F, D, 0, st));
@@ -184,7 +187,7 @@ nvfp4_status nvfp4_mlp_bwd(const nvfp4_mlp_params* p, const void* dY, const void
                            size_t workspace_bytes, nvfp4_stream stream) {
   if (!p || !dY || !saved || !dX || !dWg || !dWu || !dWd || !workspace)
     return NVFP4_ERR_INVALID_ARG;
-  if (p->flags & ~(uint32_t)NVFP4_RHT) return NVFP4_ERR_INVALID_ARG;
+  if (p->flags & ~(uint32_t)(NVFP4_RHT | NVFP4_AMAX_GIVEN)) return NVFP4_ERR_INVALID_ARG;
   const int64_t M = p->M, D = p->D, F = p->F;
   if (!dims_ok(M, D, F)) return NVFP4_ERR_SHAPE;
   Saved s;

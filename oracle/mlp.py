@@ -75,3 +75,23 @@ def mlp_bwd(dY, saved, dWg, dWu, dWd, step: int = 0):
     dWu += bf16_to_f32(_bf16_gemm(qdUc, saved["qXc"]))
     return dX, {"dH": dH, "dG": dG, "dU": dU, "qdY": qdY, "qdYc": qdYc, "qdG": qdG,
                 "qdGc": qdGc, "qdU": qdU, "qdUc": qdUc}
+
+
+def sgd_step(W, G, lr: float, zero_grad: bool = False):
+    """The optimizer step of an FP32 master weight, with the amax its next
+    16x16 quantisation takes.  The page's Figure 1 text folds the GEMMs' BF16
+    outputs into an FP32 master weight on the optimizer step, and the weights
+    are quantised under a per-tensor scale from their amax every step.  The
+    pages name no optimizer; this is plain SGD, elementwise in binary32 with
+    the product rounded before the difference (numpy float32 arithmetic
+    rounds each operation; no fused multiply-add):
+        W_new = W - lr * G,   G_new = 0 (zero_grad) or G,
+        amax  = max |W_new| over every element (the per-tensor amax of
+                W_new's 16x16 quantisation, which reduces no other way).
+    W, G: float32 arrays of one shape.  Returns (W_new, G_new, amax)."""
+    W = np.asarray(W, np.float32)
+    G = np.asarray(G, np.float32)
+    prod = np.multiply(np.float32(lr), G, dtype=np.float32)
+    W_new = np.subtract(W, prod, dtype=np.float32)
+    G_new = np.zeros_like(G) if zero_grad else G.copy()
+    return W_new, G_new, np.float32(np.abs(W_new).max())

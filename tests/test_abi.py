@@ -249,3 +249,27 @@ def test_debug_inject_rejects_unknown_bits_without_a_device(lib):
     lib.nvfp4_debug_inject.argtypes = [C.c_uint32, C.c_uint64]
     assert lib.nvfp4_debug_inject(4, 0) == 1
     assert lib.nvfp4_debug_inject(0xFFFFFFFC, 1000) == 1
+
+
+def test_sgd_step_argument_errors_before_any_launch(lib):
+    """nvfp4_sgd_step refuses bad arguments before touching the device:
+    NULL pointers, unknown flags, a non-finite rate, overlapping W and G
+    (INVALID_ARG), n <= 0 or not a multiple of 4 (SHAPE), misalignment
+    (ALIGN), a missing workspace when the amax is asked for (WORKSPACE)."""
+    f = lib.nvfp4_sgd_step
+    f.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_float, C.c_uint32, C.c_void_p,
+                  C.c_void_p, C.c_size_t, C.c_void_p]
+    INVALID, SHAPE, ALIGN, WORKSPACE = 1, 2, 3, 5
+    W, G, A, WS = 0x10000, 0x20000, 0x30000, 0x40000   # never dereferenced on these paths
+    assert f(None, G, 64, 0.1, 0, None, None, 0, None) == INVALID
+    assert f(W, None, 64, 0.1, 0, None, None, 0, None) == INVALID
+    assert f(W, G, 64, 0.1, 1, None, None, 0, None) == INVALID
+    assert f(W, G, 64, float("inf"), 0, None, None, 0, None) == INVALID
+    assert f(W, G, 64, float("nan"), 0, None, None, 0, None) == INVALID
+    assert f(W, W + 64, 64, 0.1, 0, None, None, 0, None) == INVALID    # overlapping
+    assert f(W, G, 0, 0.1, 0, None, None, 0, None) == SHAPE
+    assert f(W, G, 66, 0.1, 0, None, None, 0, None) == SHAPE
+    assert f(W + 4, G, 64, 0.1, 0, None, None, 0, None) == ALIGN
+    assert f(W, G, 64, 0.1, 0, A + 2, WS, 4096, None) == ALIGN
+    assert f(W, G, 64, 0.1, 16, A, None, 0, None) == WORKSPACE
+    assert f(W, G, 64, 0.1, 16, A, WS, 16, None) == WORKSPACE

@@ -232,3 +232,56 @@ def test_mlp_wgrad_operands_carry_the_rht(orc, mlp_run):
         plain = syn.bf16_bits_to_f32(src).astype(np.float64).T
         assert _rel(deq, T) < 0.3, (name, _rel(deq, T))
         assert _rel(deq, plain) > 0.7, (name, _rel(deq, plain))
+
+
+# ---- the optimizer step (FP32 master weight, plain SGD) -----------------------------
+def test_sgd_step_exact_on_representable_values(orc):
+    """Integers times a power of two: every product and difference is exact in
+    binary32, so the step must equal the exact FP64 result element for element,
+    and the amax the largest magnitude of it."""
+    from oracle.mlp import sgd_step
+    rng = np.random.Generator(np.random.PCG64(61))
+    W = rng.integers(-4096, 4096, (48, 64)).astype(np.float32)
+    G = rng.integers(-4096, 4096, (48, 64)).astype(np.float32)
+    for lr in (0.5, 0.25, 2.0, -1.0):
+        Wn, Gn, a = sgd_step(W, G, lr)
+        exact = W.astype(np.float64) - lr * G.astype(np.float64)
+        assert np.array_equal(Wn.astype(np.float64), exact)
+        assert np.array_equal(Gn, G)
+        assert a == np.float32(np.abs(exact).max())
+
+
+def test_sgd_step_rounds_the_product_first(orc):
+    """lr = G = 1 + 2^-23: lr * G = 1 + 2^-22 + 2^-46 rounds to 1 + 2^-22, so
+    W = 1 + 2^-22 steps exactly to 0; a fused multiply-add would leave -2^-46.
+    W = 3 with G = 0.1 (not a binary32 value times lr = 0.1) checks the
+    rounding of the difference against an FP64 evaluation of the same two
+    rounded operations."""
+    from oracle.mlp import sgd_step
+    one_ulp = np.float32(1 + 2.0 ** -23)
+    W = np.array([[np.float32(1 + 2.0 ** -22), 3.0, -0.5, 7.0]], np.float32)
+    G = np.array([[one_ulp, 0.1, 0.0, -2.0]], np.float32)
+    Wn, _, _ = sgd_step(W[:, :1], G[:, :1], float(one_ulp))
+    assert Wn[0, 0] == 0.0 and not np.signbit(Wn[0, 0])
+    Wn, _, a = sgd_step(W, G, 0.1)
+    prod = np.float32(np.float64(np.float32(0.1)) * np.float64(G[0, 1]))
+    assert Wn[0, 1] == np.float32(np.float64(W[0, 1]) - np.float64(prod))
+    assert Wn[0, 2] == np.float32(-0.5) and Wn[0, 3] == np.float32(7.0) + np.float32(0.2)
+    assert a == np.abs(Wn).max()
+
+
+def test_sgd_step_zero_grad_and_zero_rate(orc):
+    """zero_grad clears the gradient; lr = 0 leaves a weight without negative
+    zeros unchanged bit for bit; the amax equals the one the oracle's 16x16
+    quantiser takes of the updated weight (its own C reduction)."""
+    from oracle.mlp import sgd_step
+    rng = np.random.Generator(np.random.PCG64(62))
+    W = (rng.standard_normal((32, 48)) * 0.02).astype(np.float32)
+    W[W == 0] = 1e-3
+    G = (rng.standard_normal((32, 48)) * 1e-3).astype(np.float32)
+    Wn, Gn, a = sgd_step(W, G, 0.0, zero_grad=True)
+    assert np.array_equal(Wn.view(np.uint32), W.view(np.uint32))
+    assert not Gn.any()
+    Wn, _, a = sgd_step(W, G, 3e-2)
+    q = orc.quantize(Wn, orc.BLOCK_16X16, orc.EMIT_T)
+    assert a == q["amax"] == np.abs(Wn).max()
