@@ -41,6 +41,14 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # the kernel changes after the capture.
 FPROP_TRAFFIC_BYTES = 55.467776e6 + 187.944448e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
+# Warp instructions one launch of dY's one-read quantiser (row SR + column
+# RHT + SR, quant_rowcol_kernel<1, 1, 1>) executes at dY [8192, 14336], from
+# one ncu capture of that launch (inst_executed); None once the kernel
+# changes after the capture.  The kernel is bound by instruction issue, not
+# by HBM: its roofline is the issue rate of 4 schedulers per SM, one warp
+# instruction each per cycle.
+SR_ROWCOL_INSTRUCTIONS = 383331731
+SR_ROWCOL_SHAPE = (8192, 14336)  # (M, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
         "dY ~ N(0,1e-3), bf16")
@@ -405,6 +413,19 @@ def run_ours(args):
                and (args.m, args.k, args.n) == FPROP_TRAFFIC_SHAPE else None)
     q_ms = sum(kern_ms[k] for k in layer.names if k.startswith("q_"))
     q_gbs = layer.quant_bytes() / (q_ms * 1e-3) / 1e9
+    sr_issue = None
+    if SR_ROWCOL_INSTRUCTIONS is not None and (args.m, args.n) == SR_ROWCOL_SHAPE:
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+        peak_i = sms * 4 * mhz * 1e6 / 1e9  # G warp instructions / s
+        ach_i = SR_ROWCOL_INSTRUCTIONS / (kern_ms["q_dy_rowcol_rht_sr"] * 1e-3) / 1e9
+        sr_issue = {"bound": "issue",
+                    "kernel": "quant_rowcol_kernel<RHT, SR, SR>: dY's row SR + column RHT + SR",
+                    "achieved": round(ach_i, 1), "peak": round(peak_i, 1),
+                    "unit": "G warp instructions/s", "frac": round(ach_i / peak_i, 4),
+                    "instructions_per_launch": SR_ROWCOL_INSTRUCTIONS,
+                    "peak_source": f"{sms} SMs x 4 schedulers x 1 warp instruction per cycle "
+                                   f"x {mhz:g} MHz (max SM clock sampled)"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -434,7 +455,8 @@ def run_ours(args):
                      "note": "algorithmic bytes (each bf16 input read once, codes + scales "
                              "written) over quantiser time including the amax pre-passes; "
                              "frac_if_inputs_read_per_quantisation counts X and dY read once "
-                             "per quantisation (five)"},
+                             "per quantisation (five)",
+                     "sr_issue_roofline": sr_issue},
         "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "warmup": args.e2e_warmup,
