@@ -180,30 +180,42 @@ NVFP4_DEV uint32_t e2m1x2_rn(float lo, float hi) {
   return r & 0xFFu;
 }
 
-// Stochastic rounding of y onto the E2M1 grid {0,.5,1,1.5,2,3,4,6}: rounds
-// |y| up to the next grid value iff r < floor(frac * 2^32), frac =
-// (|y| - lo) / (hi - lo).  Returns the 4-bit code, sign kept; |y| >= 6
-// saturates.  Evaluated exactly and without branches on the float's bits:
-// for |y| >= 1 the grid keeps one mantissa bit and frac * 2^32 is the 22
-// bits below it shifted left by 10, so r < thr iff the 22-bit complement of
-// r's top 22 bits, added to those bits, carries into the kept bit -- adding
-// it to the whole word performs the round-up, binade changes included, and
-// the code is read off bits 22 and up.  On [0.5, 1) the same holds with 23
-// bits (the carry reaches the exponent); below 0.5 the threshold is
-// floor(|y| * 2^33), an exact power-of-two scaling.
-NVFP4_DEV uint32_t e2m1_sr(float y, uint32_t r) {
-  const uint32_t bits = __float_as_uint(y);
-  const uint32_t sign = (bits >> 28) & 8u;
-  const uint32_t a = __float_as_uint(fabsf(y));
+// Stochastic rounding of a magnitude onto the E2M1 grid {0,.5,1,1.5,2,3,4,6}:
+// a = the bits of |y|; rounds |y| up to the next grid value iff
+// r < floor(frac * 2^32), frac = (|y| - lo) / (hi - lo).  Returns the 3-bit
+// magnitude code; |y| >= 6 saturates (the caller adds the sign).  Evaluated
+// exactly and without branches on the float's bits: for |y| >= 1 the grid
+// keeps one mantissa bit and frac * 2^32 is the 22 bits below it shifted
+// left by 10, so r < thr iff the 22-bit complement of r's top 22 bits, added
+// to those bits, carries into the kept bit -- adding it to the whole word
+// performs the round-up, binade changes included, and the code is read off
+// bits 22 and up.  On [0.5, 1) the same holds with 23 bits (the carry
+// reaches the exponent); below 0.5 the threshold is floor(|y| * 2^33), an
+// exact power-of-two scaling.
+NVFP4_DEV uint32_t e2m1_sr_mag(uint32_t a, uint32_t r) {
   const bool ge1 = a >= 0x3F800000u;
   const uint32_t t = a + ((~r) >> (ge1 ? 10 : 9));
   const uint32_t code_hi = ge1 ? (t >> 22) - 252u : (t >> 23) - 125u;
   const uint32_t thr = __float2uint_rz(__fmul_rn(__uint_as_float(a), 8589934592.0f));
-  uint32_t code = a < 0x3F000000u ? (thr > r ? 1u : 0u) : code_hi;
+  const uint32_t code = a < 0x3F000000u ? (thr > r ? 1u : 0u) : code_hi;
   // |y| >= 6 (or not finite) saturates: code_hi is at least 7 there, and never
   // above 7 below it (lo = 4 rounds up to code 7 at most)
-  code = min(code, 7u);
-  return sign | code;
+  return min(code, 7u);
+}
+
+// The sign bits of eight values at the sign positions of their 4-bit codes
+// (bit 4 i + 3 = sign of v[i]): the top bytes of v[1], v[3], v[5], v[7]
+// gathered into bytes 0..3 put each sign at bit 8 k + 7; those of the even
+// elements, gathered likewise and shifted down by 4, at bit 8 k + 3.
+NVFP4_DEV uint32_t sign_nibbles8(const float (&v)[8]) {
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(v[i]);
+  const uint32_t odd =
+      __byte_perm(__byte_perm(b[1], b[3], 0x0073), __byte_perm(b[5], b[7], 0x0073), 0x5410);
+  const uint32_t even =
+      __byte_perm(__byte_perm(b[0], b[2], 0x0073), __byte_perm(b[4], b[6], 0x0073), 0x5410);
+  return (odd & 0x80808080u) | ((even >> 4) & 0x08080808u);
 }
 
 // Correctly rounded a / 6 for a >= 2^-100 without a division: the product

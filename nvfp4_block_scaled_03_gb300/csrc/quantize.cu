@@ -233,17 +233,21 @@ NVFP4_DEV void fill_enc_table(float* tab, float s_enc) {
 NVFP4_DEV float encode_factor(const float* tab, uint32_t sc) { return tab[sc & 127u]; }
 
 // 8 elements -> 32 bits of packed codes (element 0 in the lowest nibble).
+// SR takes each magnitude as |v| * enc (= |v * enc|: enc >= 0, and binary32
+// rounding is symmetric) and the eight signs from v in one gather.
 template <bool SR>
 NVFP4_DEV uint32_t encode8(const float (&v)[8], float enc, uint4 w0, uint4 w1) {
-  float y[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], enc);
   uint32_t out = 0;
   if (SR) {
     const uint32_t r[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out += e2m1_sr(y[i], r[i]) * (1u << (4 * i));  // disjoint nibbles
+    for (int i = 0; i < 8; ++i)  // disjoint nibbles
+      out += e2m1_sr_mag(__float_as_uint(__fmul_rn(fabsf(v[i]), enc)), r[i]) * (1u << (4 * i));
+    out |= sign_nibbles8(v);
   } else {
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], enc);
 #pragma unroll
     for (int i = 0; i < 4; ++i) out |= e2m1x2_rn(y[2 * i], y[2 * i + 1]) << (8 * i);
   }
