@@ -113,17 +113,15 @@ NVFP4_DEV void butterfly_local(float (&v)[N]) {
   }
 }
 
-// max |(H16 diag(s) v)_i| over one block, without the transform's x 1/4
-// (applied by the caller to its final maximum: rounding is monotone, so that
-// maximum is the same bit for bit).  Signs and butterfly stages h = 1, 2, 4
-// as in the full transform; the last stage turns each pair (a, b) into a + b
-// and a - b, and the larger magnitude of the two rounded results is exactly
-// the rounded |a| + |b| (one of them is that sum, the other is no larger),
-// so the stage is one add per pair.  v is overwritten.
-NVFP4_DEV float rht16_absmax_unscaled(float (&v)[16], uint32_t sign_bits) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if ((sign_bits >> i) & 1u) v[i] = -v[i];
+// max |(H16 diag(s) v)_i| over one block whose random signs s were applied
+// already, without the transform's x 1/4 (applied by the caller to its final
+// maximum: rounding is monotone, so that maximum is the same bit for bit).
+// Butterfly stages h = 1, 2, 4 as in the full transform; the last stage
+// turns each pair (a, b) into a + b and a - b, and the larger magnitude of
+// the two rounded results is exactly the rounded |a| + |b| (one of them is
+// that sum, the other is no larger), so the stage is one add per pair.  v is
+// overwritten.
+NVFP4_DEV float rht16_absmax_signed(float (&v)[16]) {
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
@@ -140,16 +138,28 @@ NVFP4_DEV float rht16_absmax_unscaled(float (&v)[16], uint32_t sign_bits) {
   for (int i = 0; i < 8; ++i) m = fmaxf(m, __fadd_rn(fabsf(v[i]), fabsf(v[i + 8])));
   return m;
 }
-
-// Full 16-point transform of one register-resident block: signs, stages
-// h = 1, 2, 4, 8, then x 1/4.
-NVFP4_DEV void rht16_block(float (&v)[16], uint32_t sign_bits) {
+// As rht16_absmax_signed, with the random signs applied here.
+NVFP4_DEV float rht16_absmax_unscaled(float (&v)[16], uint32_t sign_bits) {
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     if ((sign_bits >> i) & 1u) v[i] = -v[i];
+  return rht16_absmax_signed(v);
+}
+
+// The 16-point transform of one register-resident block whose random signs
+// were applied as it was loaded (rht_sign_masks): stages h = 1, 2, 4, 8,
+// then x 1/4.
+NVFP4_DEV void rht16_signed_block(float (&v)[16]) {
   butterfly_local<16>(v);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+// The transform's signs as XOR masks, one per row e of a 16-row block: bit 31
+// set where sign bit e negates that row.
+NVFP4_DEV void rht_sign_masks(uint32_t sign_bits, uint32_t (&m)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m[e] = ((sign_bits >> e) & 1u) << 31;
 }
 
 // ---------------------------------------------------------------------------

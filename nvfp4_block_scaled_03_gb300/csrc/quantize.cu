@@ -133,6 +133,19 @@ template <class G>
 NVFP4_DEV float2 lds2(const uint8_t* st, int r, int c, const float*) {
   return *reinterpret_cast<const float2*>(st + swz<G>(r, c * 4));
 }
+// As lds2, both elements negated where m has bit 31 set (one XOR of the
+// loaded word: the transform's sign of their row).
+template <class G>
+NVFP4_DEV float2 lds2s(const uint8_t* st, int r, int c, uint32_t m, const uint16_t*) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(st + swz<G>(r, c * 2)) ^ (m | (m >> 16));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <class G>
+NVFP4_DEV float2 lds2s(const uint8_t* st, int r, int c, uint32_t m, const float*) {
+  const float2 f = *reinterpret_cast<const float2*>(st + swz<G>(r, c * 4));
+  return make_float2(__uint_as_float(__float_as_uint(f.x) ^ m),
+                     __uint_as_float(__float_as_uint(f.y) ^ m));
+}
 
 // ---- bounded waits -------------------------------------------------------------
 NVFP4_DEV bool q_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned code) {
@@ -391,14 +404,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
 }
 
 // One output row (input column c0 + ol) of a COL_1X16 tile: 16 values of the
-// 16-row block j -> RHT, scale, codes, staged for the coalesced store.
+// 16-row block j (with RHT: already sign-flipped at the load) -> the
+// transform, scale, codes, staged for the coalesced store.
 template <bool RHT, bool SR>
 NVFP4_DEV void col_block(float (&v)[16], int ol, int j, bool rows_ok, int64_t c0, int64_t r0,
-                         int64_t R, int64_t C, float s_enc, const float* tab, uint32_t sign_bits,
+                         int64_t R, int64_t C, float s_enc, const float* tab,
                          const PhiloxKeys& rk, uint64_t offset, uint32_t* out_s, uint8_t* atom) {
   const int64_t col = c0 + ol;
   const bool ok = rows_ok && col < C;
-  if (RHT) rht16_block(v, sign_bits);
+  if (RHT) rht16_signed_block(v);
   float m = 0.0f;
 #pragma unroll
   for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
@@ -458,7 +472,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
   }
   const int cp = lane + 32 * (warp & 1), j = warp >> 1;
   const int64_t apr = ((R / 16) + 3) / 4;
-  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
+  uint32_t smask[16] = {};  // the transform's sign of block row e (bit 31)
+  if (RHT) rht_sign_masks(rht_sign_bits(p.seed), smask);
   int64_t k = 0;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
     const int s = (int)(k % G::kStages);
@@ -467,7 +482,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     float va[16], vb[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float2 f = lds2<G>(st, 16 * j + e, 2 * cp, static_cast<const T*>(nullptr));
+      const float2 f = lds2s<G>(st, 16 * j + e, 2 * cp, smask[e], static_cast<const T*>(nullptr));
       va[e] = f.x;
       vb[e] = f.y;
     }
@@ -480,10 +495,10 @@ __global__ void __launch_bounds__(kQThreads, 2)
     uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
     uint8_t* atom = smem + L::offExtra + buf * kBuf + kOutBytes;
     const bool rows_ok = r0 + 16 * j < R;
-    col_block<RHT, SR>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p.rk, p.offset,
+    col_block<RHT, SR>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc, tab, p.rk, p.offset,
                        out_s, atom);
-    col_block<RHT, SR>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc, tab, sign_bits, p.rk,
-                       p.offset, out_s, atom);
+    col_block<RHT, SR>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc, tab, p.rk, p.offset,
+                       out_s, atom);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_out + 8 * buf);
     if (!q_wait(bar_out + 8 * buf, (uint32_t)((k >> 1) & 1), abort_flag, 0x42u)) break;
@@ -574,7 +589,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int rr = tid >> 2, bp = tid & 3;                   // row role
   const int64_t apr_c = ((R / 16) + 3) / 4;  // atoms per 128 rows of the column operand
   const int64_t pc4_r = ((C / 16) + 3) / 4 * 4;  // padded scale columns of the row operand
-  const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
+  uint32_t smask[16] = {};  // the transform's sign of block row e (bit 31)
+  if (RHT) rht_sign_masks(rht_sign_bits(p.seed), smask);
   int64_t k = 0;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
     const int s = (int)(k % G::kStages);
@@ -583,7 +599,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
     float va[16], vb[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float2 f = lds2<G>(st, 16 * j + e, 2 * cp, static_cast<const uint16_t*>(nullptr));
+      const float2 f =
+          lds2s<G>(st, 16 * j + e, 2 * cp, smask[e], static_cast<const uint16_t*>(nullptr));
       va[e] = f.x;
       vb[e] = f.y;
     }
@@ -595,9 +612,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
     uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
     uint8_t* atom = smem + L::offExtra + buf * kBuf + kOutBytes;
     const bool rows_ok = r0 + 16 * j < R;
-    col_block<RHT, SRC>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, sign_bits, p.rk,
-                        p.col_offset, out_s, atom);
-    col_block<RHT, SRC>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, sign_bits, p.rk,
+    col_block<RHT, SRC>(va, 2 * cp, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, p.rk, p.col_offset,
+                        out_s, atom);
+    col_block<RHT, SRC>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, p.rk,
                         p.col_offset, out_s, atom);
     // ---- row operand: row r, columns cb .. cb + 31 (two blocks); its values
     // are read from the stage after the column role's, then the stage is freed
@@ -874,7 +891,16 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
     const T* base = x + jb * 16 * ld + cc * kCh;
     uint4 u[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) u[e] = __ldg(reinterpret_cast<const uint4*>(base + e * ld));
+    for (int e = 0; e < 16; ++e) {
+      // row e of the block, negated where the transform's sign bit e is set
+      const uint32_t me =
+          ((sign_bits >> e) & 1u) ? (sizeof(T) == 2 ? 0x80008000u : 0x80000000u) : 0u;
+      u[e] = __ldg(reinterpret_cast<const uint4*>(base + e * ld));
+      u[e].x ^= me;
+      u[e].y ^= me;
+      u[e].z ^= me;
+      u[e].w ^= me;
+    }
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       if (sizeof(T) == 2) {
@@ -886,8 +912,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
           b[e] = __uint_as_float(w & 0xFFFF0000u);
           if (PLAIN) mp = fmaxf(mp, fmaxf(fabsf(a[e]), fabsf(b[e])));
         }
-        m = fmaxf(m, fmaxf(rht16_absmax_unscaled(a, sign_bits),
-                           rht16_absmax_unscaled(b, sign_bits)));
+        m = fmaxf(m, fmaxf(rht16_absmax_signed(a), rht16_absmax_signed(b)));
       } else {
         float a[16];
 #pragma unroll
@@ -895,7 +920,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
           a[e] = __uint_as_float(wi == 0 ? u[e].x : wi == 1 ? u[e].y : wi == 2 ? u[e].z : u[e].w);
           if (PLAIN) mp = fmaxf(mp, fabsf(a[e]));
         }
-        m = fmaxf(m, rht16_absmax_unscaled(a, sign_bits));
+        m = fmaxf(m, rht16_absmax_signed(a));
       }
     }
   }
