@@ -373,31 +373,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTA-pair kernel: output tiles of 256 x 256 computed by a cluster of two
 // CTAs with tcgen05 cta_group::2.  CTA r loads A rows [128 r, 128 r + 128)
 // and B rows [128 r, 128 r + 128) of the tile, the scale atoms of its A rows
-// and all scale atoms of the tile's B rows; every load completes on the
-// leader's (rank 0) full barrier.  Per SM this moves two thirds of the operand
-// bytes of the single-CTA 128 x 256 tile and reads half the B operand bytes
-// from its own shared memory per MMA.
+// and all scale atoms of the tile's B rows (each CTA's MMA reads all of B's
+// scales from its own tensor memory).  The A and B loads complete on the
+// leader's (rank 0) full barrier.  Per SM this moves two thirds of the
+// operand bytes of the single-CTA 128 x 256 tile.
 //
-// A single thread pays an issue latency of about a hundred cycles per tcgen05
-// instruction, so one thread issuing a stage's 12 scale copies and 4 MMAs
-// cannot keep the tensor pipe busy.  The leader therefore splits the issue:
-// the copy warps each wait for the stage's data, issue their share of its 12
-// scale copies into both CTAs' tensor memory, then fence
-// (tcgen05.fence::before_thread_sync) and arrive on the stage's scales-ready
-// barrier; the MMA thread waits for that barrier, fences
-// (tcgen05.fence::after_thread_sync), which orders its MMAs behind those
-// copies in the tensor pipe without waiting for them to complete, and issues
-// only the MMAs and the commit that frees the stage.  A tensor-memory scale
-// slot is rewritten only after its stage was refilled, i.e. after the MMAs
-// that read it completed.  Each CTA's epilogue drains its 128 accumulator rows
-// and releases them on the leader's barrier.  NVFP4 B scales arrive as the
-// plain atoms of the tile's two 128-row blocks (38 KB a stage, 5 stages); the
-// MX formats, with fewer atoms per stage, take them as replicated images.
+// The block scales reach tensor memory in one of two ways.  NVFP4 (stored
+// scales): each CTA's scale atoms land on its own barrier, and four scale
+// warps per CTA -- one per 32-lane quarter -- read them from shared memory
+// and write them into their quarter with tcgen05.st, in the replicated
+// layout the block-scaled MMA reads; each waits for its stores
+// (tcgen05.wait::st), fences (tcgen05.fence::before_thread_sync) and arrives
+// on the leader's scales-ready barrier.  A scale copy (tcgen05.cp) runs in
+// the tensor pipe in order with the MMAs, at about 44 bytes of tensor memory
+// a cycle, so a stage's 24 KB of replicated scales took longer than its four
+// MMAs; the stores take a few tens of cycles beside them.  The MX formats
+// (copied scales): two copy warps issue the stage's tcgen05.cp copies into
+// both CTAs' tensor memory, B's scales as 4x-replicated images, and arrive
+// on the same barrier.  The MMA thread waits for the stage's data and its
+// scales, fences (tcgen05.fence::after_thread_sync) and issues only the MMAs
+// and the commit that frees the stage.  A tensor-memory scale slot is
+// rewritten only after its stage was refilled, i.e. after the MMAs that read
+// it completed.  Each CTA's epilogue drains its 128 accumulator rows and
+// releases them on the leader's barrier.  5 stages of 38 KB (NVFP4).
 // =============================================================================
 constexpr int kPairBN = 256;
 
 constexpr int kPairCopyWarps = 2;
-constexpr int kThreadsPairCp = (2 + kPairCopyWarps + 8) * 32;  // producer, MMA, copy, epilogue
 
 // Operand formats of the pair kernel.  Every format stages 128 bytes of K per
 // row and issues four MMAs of 32 bytes of K per stage; the scale atoms (128
@@ -409,6 +411,22 @@ struct PairFmt {
   static constexpr int kAtoms = FMT == kFmtNVF4 ? 4 : (FMT == kFmtMXF4 ? 2 : 1);  // per stage
   static constexpr int kStageK = FMT == kFmtMXF8 ? 128 : 256;  // K elements per stage
   static constexpr int kMmaPerAtom = 4 / kAtoms;
+};
+
+// Warp roles of a pair CTA.  With the scales copied (IMG, the MX formats):
+// 12 warps -- producer, MMA, two copy warps, eight epilogue warps.  With the
+// scales stored (ST, NVFP4): 16 warps in four warpgroups -- warpgroup 0 the
+// producer, the MMA warp and two idle warps; warpgroup 1 four scale warps,
+// one per 32-lane quarter; warpgroups 2-3 the epilogue.  With 16 warps a
+// sub-partition holds four, so each starts at 128 registers; warpgroups 0-1
+// hand registers to the epilogue (setmaxnreg).
+template <bool ST>
+struct PairRoles {
+  static constexpr int kEpi0 = ST ? 8 : 2 + kPairCopyWarps;  // first of 8 epilogue warps
+  static constexpr int kThreads = (kEpi0 + 8) * 32;
+  static constexpr int kRegsIssue = 96, kRegsEpilogue = 160;  // ST only
+  static constexpr int kSplitRegs = 2 * 128 * kRegsIssue + 2 * 128 * kRegsEpilogue;
+  static_assert(!ST || kSplitRegs <= kThreads * 128, "register split exceeds the launch's");
 };
 
 // Instruction descriptor of the MX block-scaled MMAs: element format code for
@@ -448,6 +466,7 @@ NVFP4_DEV void tc_mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, u
 
 template <int STAGES, int FMT, bool IMG>
 struct PairSmem {
+  static constexpr bool kST = FMT == kFmtNVF4 && !IMG;  // scales through tcgen05.st
   static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
@@ -458,13 +477,18 @@ struct PairSmem {
   // tensor memory
   static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
   static constexpr uint32_t kSFB = IMG ? kAt * 4096 : kAt * 1024;
-  static constexpr uint32_t kStageTx = 2 * (kA + kB + kSFA + kSFB);  // both CTAs
+  // bytes counted on the leader's full barrier: both CTAs' A and B, and with
+  // the scales copied also their scale atoms (stored scales land on each
+  // CTA's own scale barrier)
+  static constexpr uint32_t kStageTx = 2 * (kA + kB) + (kST ? 0 : 2 * (kSFA + kSFB));
   static constexpr uint32_t offA = 0;
   static constexpr uint32_t offB = offA + STAGES * kA;
   static constexpr uint32_t offSFA = offB + STAGES * kB;
   static constexpr uint32_t offSFB = offSFA + STAGES * kSFA;
   static constexpr uint32_t offBar = offSFB + STAGES * kSFB;
-  static constexpr uint32_t kNumBars = 3 * STAGES + 3 + kPairCopyWarps;  // full, empty, scales-ready, acc x2, drains
+  // full, empty, scales-ready, scales-landed (ST) per stage; acc full, acc
+  // empty; drains (MMA warp, copy warps)
+  static constexpr uint32_t kNumBars = 4 * STAGES + 3 + kPairCopyWarps;
   static constexpr uint32_t offMisc = offBar + kNumBars * 8;
   // bf16 output staging for tensor stores: one box of 32 rows x 64 bytes per
   // epilogue warp
@@ -496,13 +520,16 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
 }
 
 template <int STAGES, int DMODE, int FMT, bool IMG>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
+__global__ void __cluster_dims__(2, 1, 1)
+__launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
                           const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
   using L = PairSmem<STAGES, FMT, IMG>;
+  constexpr bool ST = L::kST;
+  using R = PairRoles<ST>;
   constexpr int kAt = PairFmt<FMT>::kAtoms;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -512,7 +539,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto sf_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  const uint32_t acc_full = bar0 + 8u * (3 * STAGES);
+  auto scf_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // ST: this CTA's scales
+  const uint32_t acc_full = bar0 + 8u * (4 * STAGES);
   const uint32_t acc_empty = acc_full + 8;
   const uint32_t drain_bar = acc_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
@@ -530,7 +558,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(sf_bar(s), kPairCopyWarps);
+      mbar_init(sf_bar(s), ST ? 8 : kPairCopyWarps);  // ST: four scale warps per CTA
+      mbar_init(scf_bar(s), 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
@@ -548,6 +577,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < R::kEpi0) {
+  // issue warps (the register hint sits inside the branch so that the code it
+  // governs is known to the register allocator)
+  if constexpr (ST) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kRegsIssue));
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -571,6 +604,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
           tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
           tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
                            (b_rb0 + (int)rank) * 128);
+          if (ST) {
+            // this CTA's scale atoms (its A rows' and the tile's B rows', 128-byte
+            // rows, 4 per atom) on its own barrier, for its scale warps
+            mbar_arrive_expect_tx(scf_bar(s), L::kSFA + L::kSFB);
+            tma_load_2d(sbase + L::offSFA + s * L::kSFA, &tmSFA, scf_bar(s), 0,
+                        (a_rb * args.kg + kb * kAt) * 4);
+            tma_load_2d(sbase + L::offSFB + s * L::kSFB, &tmSFB, scf_bar(s), 0,
+                        (b_rb0 * args.kg + kb * kAt) * 4);
+            tma_load_2d(sbase + L::offSFB + s * L::kSFB + kAt * 512, &tmSFB, scf_bar(s), 0,
+                        ((b_rb0 + 1) * args.kg + kb * kAt) * 4);
+            if (++s == STAGES) { s = 0; ph ^= 1u; }
+            continue;
+          }
           // scale atoms as 128-byte rows (4 per atom)
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
                            (a_rb * args.kg + kb * kAt) * 4);
@@ -591,7 +637,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
         }
       }
     }
-  } else if (warp >= 2 && warp < 2 + kPairCopyWarps) {
+  } else if (ST && warp >= 4) {
+    // ------------------------------------------------------------ scale warps
+    // Warp q (= warp % 4) stores each stage's 12 scale atoms into its 32-lane
+    // quarter of this CTA's tensor memory: lane i gets row i (16 bytes, 4
+    // columns) of A's atoms j (columns 4 j ..) and of B's atoms j of both
+    // row blocks (16 + 8 j .., 20 + 8 j ..) -- the layout the block-scaled
+    // MMA reads, which the four quarters all hold.  The stores are waited
+    // for and fenced (tcgen05.fence::before_thread_sync) before the arrive;
+    // the MMA thread's fence after its wait orders its MMAs behind them.
+    const int q = warp & 3;
+    const uint32_t sf_leader = mapa_shared(sf_bar(0), 0);
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!wait_bounded_pair(scf_bar(s), ph, abort_flag, peer_abort, 0x26u)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sa = smem + L::offSFA + s * L::kSFA + lane * 16;
+        const uint8_t* sb = smem + L::offSFB + s * L::kSFB + lane * 16;
+        uint32_t v[12 * kAt];
+#pragma unroll
+        for (int j = 0; j < kAt; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sa + j * 512);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sb + j * 512);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sb + (kAt + j) * 512);
+          v[4 * j] = a.x;
+          v[4 * j + 1] = a.y;
+          v[4 * j + 2] = a.z;
+          v[4 * j + 3] = a.w;
+          v[4 * kAt + 8 * j] = b0.x;
+          v[4 * kAt + 8 * j + 1] = b0.y;
+          v[4 * kAt + 8 * j + 2] = b0.z;
+          v[4 * kAt + 8 * j + 3] = b0.w;
+          v[4 * kAt + 8 * j + 4] = b1.x;
+          v[4 * kAt + 8 * j + 5] = b1.y;
+          v[4 * kAt + 8 * j + 6] = b1.z;
+          v[4 * kAt + 8 * j + 7] = b1.w;
+        }
+        const uint32_t taddr =
+            tmem + ((uint32_t)(32 * q) << 16) + L::kSfCol0 + s * L::kSfColsPerStage;
+#pragma unroll
+        for (int c = 0; c < 12 * kAt; c += 16) tmem_st16(taddr + c, v + c);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        // relaxed: the stores have completed (wait::st) and are fenced; the
+        // thread published nothing else
+        if (lane == 0) mbar_arrive_cluster_relaxed(sf_leader + 8u * s);
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else if (!ST && warp >= 2 && warp < 2 + kPairCopyWarps) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- scale copies
       // the stage's copies: A's atom j (index j) and B's image of atom j (both
@@ -652,8 +751,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          // the copy warps observed the stage's data and issued its scale copies
-          if (!wait_bounded_pair(sf_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
+          // the copy warps observed the stage's data and issued its scale
+          // copies; with stored scales the stage's A and B are waited for
+          // here and the scales on the scale warps' barrier
+          if ((ST && !wait_bounded_pair(full_bar(s), ph, abort_flag, peer_abort, 0x24u)) ||
+              !wait_bounded_pair(sf_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
             ok = false;
             break;
           }
@@ -686,10 +788,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPairCp, 1)
         wait_drain(drain_bar, 0);
       }
     }
+  }
   } else {
     // -------------------------------------------------------------- epilogue
+    if constexpr (ST)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kRegsEpilogue));
     constexpr int kCols = kPairBN / 2, kChunks = kCols / 32;
-    const int ew = warp - 2 - kPairCopyWarps;  // epilogue warp 0..7
+    const int ew = warp - R::kEpi0;  // epilogue warp 0..7
     const int q = warp & 3, h = ew >> 2;
     const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
     const float alpha =
@@ -854,11 +959,21 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
                          cudaStream_t stream) {
   using L = PairSmem<STAGES, FMT, IMG>;
   auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE, FMT, IMG>;
+  using R = PairRoles<L::kST>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
         cudaSuccess)
       return NVFP4_ERR_CUDA;
+    if (L::kST) {
+      // setmaxnreg.inc waits until the registers it asks for are free in the
+      // block's launch allotment: refuse a build whose register count at
+      // launch cannot cover the split (it would wait forever)
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
+          fa.numRegs * R::kThreads < R::kSplitRegs)
+        return NVFP4_ERR_CUDA;
+    }
     configured = true;
   }
   // persistent grid: as many pairs as can be resident at once (cluster
@@ -867,7 +982,7 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   if (max_pairs == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(kThreadsPairCp);
+    cfg.blockDim = dim3(R::kThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -882,7 +997,7 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   }
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
-  kern<<<grid, kThreadsPairCp, L::kAlloc, stream>>>(ma, mb, msa, msb, md, a);
+  kern<<<grid, R::kThreads, L::kAlloc, stream>>>(ma, mb, msa, msb, md, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
