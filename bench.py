@@ -437,7 +437,8 @@ def run_ours(args):
                    "l2": "flushed before every timed step, untimed: 256 MiB device write, then 256 MiB device read (L2 starts cold and clean)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
-                     "kernel": "gemm_nvf4_pair_kernel, FPROP launch (one 2MNK GEMM per launch)",
+                     "kernel": "gemm_nvf4_pair384_kernel (256 x 384 CTA-pair tiles), FPROP "
+                               "launch (one 2MNK GEMM per launch)",
                      "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
                      "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)",

@@ -325,13 +325,17 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tenso
 /* Output-tile configurations of nvfp4_gemm_ex. */
 enum {
   NVFP4_TILE_AUTO = 0,          /* 128 x 128 when N <= 128; else the CTA pair when its     *
-                                 * 256 x 256 tiles number at least half the SMs; else      *
-                                 * 128 x 256 on one SM                                     */
+                                 * 256 x 256 tiles number at least half the SMs (256 x 384 *
+                                 * where its rounds of tiles per pair cost less, not with  *
+                                 * NVFP4_D_BF16_ADD_C); else 128 x 256 on one SM           */
   NVFP4_TILE_128X128 = 1,       /* one SM per 128 x 128 tile                               */
   NVFP4_TILE_128X256 = 2,       /* one SM per 128 x 256 tile                               */
   NVFP4_TILE_PAIR_256X256 = 3,  /* a cluster of two SMs per 256 x 256 tile (cta_group::2) */
   /* 4 is retired (rejected with NVFP4_ERR_INVALID_ARG)                                    */
-  NVFP4_TILE_128X256_K128 = 5   /* one SM per 128 x 256 tile, 8 stages of K = 128          */
+  NVFP4_TILE_128X256_K128 = 5,  /* one SM per 128 x 256 tile, 8 stages of K = 128          */
+  NVFP4_TILE_PAIR_256X384 = 6   /* a cluster of two SMs per 256 x 384 tile: an N = 256 and *
+                                 * an N = 128 MMA per K step, 4 stages; not with           *
+                                 * NVFP4_D_BF16_ADD_C (NVFP4_ERR_INVALID_ARG)              */
 };
 
 /* As nvfp4_gemm with an explicit output-tile configuration (NVFP4_TILE_*).

@@ -25,7 +25,8 @@ RHT, SR, EMIT_T, AMAX_GIVEN = 1, 2, 4, 8
 D_BF16, D_F32_ACCUM, D_BF16_ADD_C = 0, 1, 2
 MXFP4, MXFP8 = 0, 1
 MX_ROW, MX_COL = 0, 1
-TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256, TILE_128X256_K128 = 0, 1, 2, 3, 5
+(TILE_AUTO, TILE_128X128, TILE_128X256, TILE_PAIR_256X256, TILE_128X256_K128,
+ TILE_PAIR_256X384) = 0, 1, 2, 3, 5, 6
 
 
 class NVFP4Error(RuntimeError):

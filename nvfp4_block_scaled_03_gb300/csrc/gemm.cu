@@ -193,6 +193,59 @@ NVFP4_DEV void prefetch_l2_row(const void* p, int bytes) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(c + o)));
 }
 
+// Epilogue helper: one warp's 32 rows x 32 bf16 columns (lane = row, 16
+// packed pairs) into its staging box, then one tensor store at (x, y).  The
+// box is rewritten only after the previous store has read it; the 16-byte
+// pieces are rotated so a warp's writes hit distinct banks.
+NVFP4_DEV void store_box_bf16(uint8_t* box, int lane, const uint32_t (&pk)[16],
+                              const CUtensorMap* tmD, int32_t x, int32_t y) {
+  if (lane == 0) bulk_wait_group_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int pc = 0; pc < 4; ++pc) {
+    const int piece = (pc + (lane >> 1)) & 3;
+    uint4 v;
+    switch (piece) {
+      case 0: v = make_uint4(pk[0], pk[1], pk[2], pk[3]); break;
+      case 1: v = make_uint4(pk[4], pk[5], pk[6], pk[7]); break;
+      case 2: v = make_uint4(pk[8], pk[9], pk[10], pk[11]); break;
+      default: v = make_uint4(pk[12], pk[13], pk[14], pk[15]); break;
+    }
+    *reinterpret_cast<uint4*>(box + lane * 64 + piece * 16) = v;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmD, smem_u32(box), x, y);
+    bulk_commit_group();
+  }
+}
+
+// The FP32 fold from 32 bf16 results already rounded and packed in pairs:
+// D[row, col0 + i] += float(bf16 result i), the same single FP32 add as
+// store_row_chunk's F32_ACCUM branch.
+NVFP4_DEV void fold_row_chunk_packed(const GemmArgs& a, int64_t row, int64_t col0,
+                                     const uint32_t (&pk)[16]) {
+  float* D = static_cast<float*>(a.D) + row * a.N + col0;
+#pragma unroll
+  for (int g0 = 0; g0 < 8; g0 += 4) {
+    float4 d[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (col0 + (g0 + g) * 4 < a.N) d[g] = *reinterpret_cast<const float4*>(D + (g0 + g) * 4);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col0 + (g0 + g) * 4 >= a.N) break;
+      const uint32_t p0 = pk[(g0 + g) * 2], p1 = pk[(g0 + g) * 2 + 1];
+      d[g].x = __fadd_rn(d[g].x, __uint_as_float(p0 << 16));
+      d[g].y = __fadd_rn(d[g].y, __uint_as_float(p0 & 0xFFFF0000u));
+      d[g].z = __fadd_rn(d[g].z, __uint_as_float(p1 << 16));
+      d[g].w = __fadd_rn(d[g].w, __uint_as_float(p1 & 0xFFFF0000u));
+      *reinterpret_cast<float4*>(D + (g0 + g) * 4) = d[g];
+    }
+  }
+}
+
 template <int BN, int STAGES, int DMODE, int BKB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -885,6 +938,315 @@ __launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
   }
 }
 
+
+// =============================================================================
+// Wide CTA-pair kernel (NVFP4): output tiles of 256 x 384.  Per K step two
+// MMAs -- N = 256 into accumulator columns [0, 256), issued by warp 1, and
+// N = 128 into [256, 384), issued by warp 2 -- from one A and one B stage:
+// CTA r holds A rows [128 r, 128 r + 128), B rows [128 r, 128 r + 128) (the
+// first MMA's half) and [256 + 64 r, 256 + 64 r + 64) (the second's) of the
+// tile, its A rows' scale atoms and all three of the tile's B row blocks'.
+// A stage is 48 KB per SM for 1.5x the work of a 256-wide stage's 38 KB; the
+// scales are stored by the four scale warps of each CTA, as in the pair
+// kernel.  The 384 accumulator columns leave 128 of tensor memory: two scale
+// slots of 64 columns ([B's third row block: 4 per atom] [A: 4 per atom]
+// [B's first two row blocks: 8 per atom]); a slot is rewritten once the MMAs
+// two stages back completed (this CTA's empty barrier of that stage), and
+// shared memory holds 4 stages.  Each epilogue warp drains 192 columns,
+// rounding each 32-column chunk to bf16 as it arrives (96 packed registers),
+// then stores them (bf16 out) or folds them into FP32 (F32_ACCUM).  16
+// warps: warpgroup 0 = producer, the two MMA warps, an idle warp;
+// warpgroup 1 = scale warps; warpgroups 2-3 = epilogue (setmaxnreg split).
+// =============================================================================
+struct Pair384Smem {
+  static constexpr int kStages = 4, kAt = 4;
+  static constexpr uint32_t kA = 128 * kBKBytes, kB = 192 * kBKBytes;
+  static constexpr uint32_t kSFA = kAt * 512, kSFB = kAt * 512 * 3;
+  static constexpr uint32_t offA = 0, offB = kStages * kA, offSFA = offB + kStages * kB;
+  static constexpr uint32_t offSFB = offSFA + kStages * kSFA, offBar = offSFB + kStages * kSFB;
+  // full, empty, scales-ready, scales-landed per stage; acc full, acc empty;
+  // a drain barrier per MMA warp
+  static constexpr uint32_t kNumBars = 4 * kStages + 4;
+  static constexpr uint32_t offMisc = offBar + kNumBars * 8;
+  static constexpr uint32_t kStoreBox = 32 * 64;
+  static constexpr uint32_t offStore = (offMisc + 16 + 127) / 128 * 128;
+  static constexpr uint32_t kBytes = offStore + 8 * kStoreBox;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static constexpr uint32_t kSfCol0 = 384, kSlotCols = 64;
+  static constexpr uint32_t kColB2 = 0, kColA = 16, kColB01 = 32;  // inside a slot
+  static constexpr int kSlots = 2;
+  static constexpr int kThreads = 512;
+  static constexpr int kRegsIssue = 88, kRegsEpilogue = 168;
+  static constexpr int kSplitRegs = 2 * 128 * kRegsIssue + 2 * 128 * kRegsEpilogue;
+  static_assert(kSfCol0 + kSlots * kSlotCols <= kTmemCols, "tensor memory overflow");
+  static_assert(kAlloc <= 232448, "shared memory overflow");
+  static_assert(kSplitRegs <= kThreads * 128, "register split exceeds the launch's");
+};
+
+template <int DMODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair384Smem::kThreads, 1)
+    gemm_nvf4_pair384_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmB2,
+                             const __grid_constant__ CUtensorMap tmSFA,
+                             const __grid_constant__ CUtensorMap tmSFB,
+                             const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
+  static_assert(DMODE != NVFP4_D_BF16_ADD_C, "384-wide tiles take no bf16 C input");
+  using L = Pair384Smem;
+  constexpr int S = L::kStages, kAt = L::kAt;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::offBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto sf_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto scf_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  const uint32_t acc_full = bar0 + 8u * (4 * S);
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t drain_bar = acc_full + 16;  // MMA warps 1 and 2
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + L::offMisc + 4), rank ^ 1u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = (args.K + 255) / 256;
+  const int num_tiles = args.num_m_blk * args.num_n_blk;  // 256 x 384 tiles
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 2);  // one commit per MMA warp
+      mbar_init(sf_bar(s), 8);     // four scale warps in each CTA
+      mbar_init(scf_bar(s), 1);
+    }
+    mbar_init(acc_full, 2);
+    mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA
+    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar + 8, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kRegsIssue));
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmB2);
+      prefetch_tmap(&tmSFA);
+      prefetch_tmap(&tmSFB);
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+        const int a_rb = m_blk * 2 + (int)rank;  // this CTA's 128-row block of A
+        const int b_rb0 = n_blk * 3;             // the tile's first 128-row block of B
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded_pair(empty_bar(s), ph ^ 1u, abort_flag, peer_abort, 0x11u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(s), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * (L::kA + L::kB));
+          tma_load_2d_pair(sbase + L::offA + s * L::kA, &tmA, fb, kb * kBKBytes, a_rb * 128);
+          tma_load_2d_pair(sbase + L::offB + s * L::kB, &tmB, fb, kb * kBKBytes,
+                           n_blk * 384 + (int)rank * 128);
+          tma_load_2d_pair(sbase + L::offB + s * L::kB + 128 * kBKBytes, &tmB2, fb,
+                           kb * kBKBytes, n_blk * 384 + 256 + (int)rank * 64);
+          // this CTA's scale atoms on its own barrier (a block past N reads as zeros)
+          mbar_arrive_expect_tx(scf_bar(s), L::kSFA + L::kSFB);
+          tma_load_2d(sbase + L::offSFA + s * L::kSFA, &tmSFA, scf_bar(s), 0,
+                      (a_rb * args.kg + kb * kAt) * 4);
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+            tma_load_2d(sbase + L::offSFB + s * L::kSFB + i * kAt * 512, &tmSFB, scf_bar(s), 0,
+                        ((b_rb0 + i) * args.kg + kb * kAt) * 4);
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // give copies already issued time to land before exit
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA
+      const bool second = warp == 2;
+      const uint32_t idesc = second ? idesc_nvf4(256, 128) : idesc_nvf4(256, 256);
+      const uint32_t d_tmem = tmem + (second ? 256u : 0u);
+      const uint32_t b_off = second ? 128u * kBKBytes : 0u;
+      const uint32_t sfb_col = second ? L::kColB2 : L::kColB01;
+      const uint32_t sfb_step = second ? 4u : 8u;  // columns per atom
+      const uint32_t my_drain = drain_bar + (second ? 8u : 0u);
+      uint32_t s = 0, ph = 0, acc_ph = 0, it = 0;
+      bool ok = true, issued = false;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        if (!wait_bounded_pair(acc_empty, acc_ph ^ 1u, abort_flag, peer_abort, 0x22u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          if (!wait_bounded_pair(full_bar(s), ph, abort_flag, peer_abort, 0x24u) ||
+              !wait_bounded_pair(sf_bar(s), ph, abort_flag, peer_abort, 0x23u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nmma = min(kAt, args.kg - kb * kAt);
+          const uint32_t slot = tmem + L::kSfCol0 + (it % L::kSlots) * L::kSlotCols;
+          const uint32_t a0 = sbase + L::offA + s * L::kA;
+          const uint32_t b0 = sbase + L::offB + s * L::kB + b_off;
+          for (int j = 0; j < nmma; ++j)
+            tc_mma_pair_nvf4(d_tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(b0 + 32 * j),
+                             idesc, slot + L::kColA + 4 * j, slot + sfb_col + sfb_step * j,
+                             (kb | j) != 0 ? 1u : 0u);
+          issued = true;
+          tc_commit_pair(empty_bar(s), 3);
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair(acc_full, 3);
+        acc_ph ^= 1u;
+      }
+      if (!ok && issued) {
+        tc_commit_pair(my_drain, 1);
+        wait_drain(my_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ scale warps
+    // as in the pair kernel, 16 atoms a stage (B's third row block, A, B's
+    // first two), into the slot of the stage's iteration
+    const int q = warp & 3;
+    const uint32_t sf_leader = mapa_shared(sf_bar(0), 0);
+    uint32_t s = 0, ph = 0, it = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if (!wait_bounded_pair(scf_bar(s), ph, abort_flag, peer_abort, 0x26u)) {
+          ok = false;
+          break;
+        }
+        if (it >= (uint32_t)L::kSlots) {
+          // the slot's previous stage: its MMAs completed (its empty barrier)
+          const uint32_t prev = it - L::kSlots;
+          if (!wait_bounded_pair(empty_bar(prev % S), (prev / S) & 1u, abort_flag, peer_abort,
+                                 0x25u)) {
+            ok = false;
+            break;
+          }
+        }
+        const uint8_t* sa = smem + L::offSFA + s * L::kSFA + lane * 16;
+        const uint8_t* sb = smem + L::offSFB + s * L::kSFB + lane * 16;
+        uint32_t v[64];
+#pragma unroll
+        for (int j = 0; j < kAt; ++j) {
+          const uint4 b2 = *reinterpret_cast<const uint4*>(sb + (2 * kAt + j) * 512);
+          const uint4 a = *reinterpret_cast<const uint4*>(sa + j * 512);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sb + j * 512);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sb + (kAt + j) * 512);
+          const uint32_t w[16] = {b2.x, b2.y, b2.z, b2.w, a.x, a.y, a.z, a.w,
+                                  b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[L::kColB2 + 4 * j + e] = w[e];
+            v[L::kColA + 4 * j + e] = w[4 + e];
+            v[L::kColB01 + 8 * j + e] = w[8 + e];
+            v[L::kColB01 + 8 * j + 4 + e] = w[12 + e];
+          }
+        }
+        const uint32_t taddr =
+            tmem + ((uint32_t)(32 * q) << 16) + L::kSfCol0 + (it % L::kSlots) * L::kSlotCols;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) tmem_st16(taddr + c, v + c);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(sf_leader + 8u * s);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+  }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kRegsEpilogue));
+    constexpr int kCols = 192, kChunks = kCols / 32;
+    const int ew = warp - 8;  // epilogue warp 0..7
+    const int q = warp & 3, h = ew >> 2;
+    const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
+    const float alpha = __fmul_rn(__ldg(args.sdec_a), __ldg(args.sdec_b));
+    uint8_t* stage_out = smem + L::offStore + ew * L::kStoreBox;
+    if (DMODE == NVFP4_D_BF16 && lane == 0) prefetch_tmap(&tmD);
+    uint32_t acc_ph = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
+      const int64_t row = (int64_t)m_blk * 256 + rank * 128 + q * 32 + lane;
+      const int32_t row0 = m_blk * 256 + (int)rank * 128 + q * 32;
+      if (DMODE == NVFP4_D_F32_ACCUM) {  // this warp's rows of D into L2 while the MMAs run
+        const int64_t col0 = (int64_t)n_blk * 384 + h * kCols;
+        if (row < args.M && col0 < args.N) {
+          const int64_t ncol = args.N - col0 < kCols ? args.N - col0 : kCols;
+          prefetch_l2_row(static_cast<const char*>(args.D) + (row * args.N + col0) * 4,
+                          (int)(ncol * 4));
+        }
+      }
+      if (!wait_bounded_pair(acc_full, acc_ph, abort_flag, peer_abort, 0x33u)) break;
+      tc_fence_after();
+      uint32_t pk[kChunks][16];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kCols + c * 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[c][e] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * e]), alpha),
+                                 __fmul_rn(__uint_as_float(r[2 * e + 1]), alpha));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+      acc_ph ^= 1u;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int64_t col0 = (int64_t)n_blk * 384 + h * kCols + c * 32;
+        if (DMODE == NVFP4_D_BF16) {
+          store_box_bf16(stage_out, lane, pk[c], &tmD, (int32_t)col0, row0);
+        } else if (row < args.M && col0 < args.N) {
+          fold_row_chunk_packed(args, row, col0, pk[c]);
+        }
+      }
+    }
+    if (DMODE == NVFP4_D_BF16 && lane == 0) bulk_wait_group<0>();  // stores done before exit
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ---- host side -----------------------------------------------------------------
 EncodeTiledFn encode_fn() { return tensor_map_encoder(); }
 
@@ -1001,6 +1363,49 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+
+template <int DMODE>
+nvfp4_status launch_pair384(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2,
+                            const CUtensorMap& msa, const CUtensorMap& msb, const CUtensorMap& md,
+                            const GemmArgs& a, int sms, cudaStream_t stream) {
+  using L = Pair384Smem;
+  auto kern = gemm_nvf4_pair384_kernel<DMODE>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    // setmaxnreg.inc waits until the registers it asks for are free in the
+    // block's launch allotment: refuse a build whose register count at launch
+    // cannot cover the split (it would wait forever)
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs * L::kThreads < L::kSplitRegs)
+      return NVFP4_ERR_CUDA;
+    configured = true;
+  }
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+    max_pairs = std::min(n, sms / 2);
+  }
+  const int tiles = a.num_m_blk * a.num_n_blk;
+  const int grid = 2 * std::min(tiles, max_pairs);
+  kern<<<grid, L::kThreads, L::kAlloc, stream>>>(ma, mb, mb2, msa, msb, md, a);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 template <int BN, int STAGES, int DMODE, int BKB>
 nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int sms,
                     cudaStream_t stream) {
@@ -1088,8 +1493,10 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   if (a_view < 0 || a_view > 1 || b_view < 0 || b_view > 1) return NVFP4_ERR_INVALID_ARG;
   if (d_mode < NVFP4_D_BF16 || d_mode > NVFP4_D_BF16_ADD_C) return NVFP4_ERR_INVALID_ARG;
   if (d_mode == NVFP4_D_BF16_ADD_C && !C) return NVFP4_ERR_INVALID_ARG;
-  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_128X256_K128 || tile == 4)
+  if (tile < NVFP4_TILE_AUTO || tile > NVFP4_TILE_PAIR_256X384 || tile == 4)
     return NVFP4_ERR_INVALID_ARG;  // 4: a retired configuration
+  if (tile == NVFP4_TILE_PAIR_256X384 && d_mode == NVFP4_D_BF16_ADD_C)
+    return NVFP4_ERR_INVALID_ARG;
   const void* a_codes = a_view ? A->codes_t : A->codes;
   const void* a_sf = a_view ? A->scales_t : A->scales;
   const void* b_codes = b_view ? B->codes_t : B->codes;
@@ -1111,11 +1518,22 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
 
   if (tile == NVFP4_TILE_AUTO) {
     // the CTA pair when its 256 x 256 tiles still give every pair of SMs
-    // work; smaller problems keep more, smaller tiles
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (N <= 128) tile = NVFP4_TILE_128X128;
-    else if (pair_tiles >= dev.sm_count / 2) tile = NVFP4_TILE_PAIR_256X256;
-    else tile = NVFP4_TILE_128X256;
+    // work; smaller problems keep more, smaller tiles.  Between the pair's
+    // two widths, the one whose rounds of tiles per pair cost less: a
+    // 384-wide tile took 1.2x the time of a 256-wide one on the Llama-3-8B
+    // shapes (same K); bf16 C input stays on the 256-wide tile.
+    const int64_t pairs = std::max(1, dev.sm_count / 2);
+    const int64_t mt = (M + 255) / 256;
+    const int64_t t256 = mt * ((N + 255) / 256), t384 = mt * ((N + 383) / 384);
+    if (N <= 128) {
+      tile = NVFP4_TILE_128X128;
+    } else if (t256 >= pairs) {
+      const int64_t w256 = (t256 + pairs - 1) / pairs, w384 = (t384 + pairs - 1) / pairs;
+      tile = (d_mode != NVFP4_D_BF16_ADD_C && 6 * w384 < 5 * w256) ? NVFP4_TILE_PAIR_256X384
+                                                                  : NVFP4_TILE_PAIR_256X256;
+    } else {
+      tile = NVFP4_TILE_128X256;
+    }
   }
   GemmArgs a;
   a.sfa = static_cast<const uint8_t*>(a_sf);
@@ -1131,6 +1549,26 @@ nvfp4_status gemm_impl(const nvfp4_tensor* A, int32_t a_view, const nvfp4_tensor
   a.nrb_b = (int)((N + 127) / 128);
   a.nrb_a = (int)((M + 127) / 128);
   CUtensorMap ma, mb;
+  if (tile == NVFP4_TILE_PAIR_256X384) {
+    // B's last 128 tile rows arrive as 64-row boxes, one per CTA
+    CUtensorMap mb2, msa, msb, md;
+    if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||
+        !make_code_map(&mb2, b_codes, N, K / 2, 64) ||
+        !make_sf_map(&msa, a_sf, swizzled_scale_bytes(M, K)) ||
+        !make_sf_map(&msb, b_sf, swizzled_scale_bytes(N, K)))
+      return NVFP4_ERR_CUDA;
+    if (d_mode == NVFP4_D_BF16) {
+      if (!make_out_map(&md, D, M, N)) return NVFP4_ERR_CUDA;
+    } else {
+      md = ma;
+    }
+    a.num_m_blk = (int)((M + 255) / 256);
+    a.num_n_blk = (int)((N + 383) / 384);
+    return d_mode == NVFP4_D_BF16
+               ? launch_pair384<NVFP4_D_BF16>(ma, mb, mb2, msa, msb, md, a, dev.sm_count, stream)
+               : launch_pair384<NVFP4_D_F32_ACCUM>(ma, mb, mb2, msa, msb, md, a, dev.sm_count,
+                                                   stream);
+  }
   if (tile == NVFP4_TILE_PAIR_256X256) {
     CUtensorMap msa, msb, md;
     if (!make_code_map(&ma, a_codes, M, K / 2, 128) || !make_code_map(&mb, b_codes, N, K / 2, 128) ||

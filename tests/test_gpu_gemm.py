@@ -43,7 +43,7 @@ def _gemms(orc, L):
     return {"FPROP": (L["X"], L["W"]), "DGRAD": (L["dY"], Wt), "WGRAD": (L["dYc"], L["Xc"])}
 
 
-@pytest.mark.parametrize("tile", [1, 2, 3, 5])
+@pytest.mark.parametrize("tile", [1, 2, 3, 5, 6])
 @pytest.mark.parametrize("M,K,N", [(128, 256, 512), (208, 192, 144), (320, 1024, 272),
                                    (128, 64, 16), (320, 576, 1040)])
 def test_gemm_small(nv, orc, M, K, N, tile):
@@ -99,26 +99,64 @@ def test_gemm_output_modes(nv, orc):
     nv.check_device_errors()
 
 
+@pytest.mark.parametrize("tile", [3, 6])
 @pytest.mark.parametrize("M,K,N", [(512, 256, 784), (768, 512, 512), (512, 320, 1168)])
-def test_gemm_output_modes_pair_kernel(nv, orc, M, K, N):
-    """The fold into FP32 and the bf16 add on the CTA-pair kernel (the large-
-    shape path), with a ragged last tile: F32_ACCUM equals W0 + float(D)
-    exactly, D the bf16 output of the same kernel; ADD_C is within the GEMM
-    tolerance of the FP64 product plus C."""
+def test_gemm_output_modes_pair_kernel(nv, orc, M, K, N, tile):
+    """The fold into FP32 and the bf16 add on the CTA-pair kernels (the large-
+    shape path: 256- and 384-wide tiles), with a ragged last tile: F32_ACCUM
+    equals W0 + float(D) exactly, D the bf16 output of the same kernel; ADD_C
+    is within the GEMM tolerance of the FP64 product plus C on the 256-wide
+    tile and refused on the 384-wide one."""
     import torch
     L = _layer(orc, M, K, N)
     a, b = L["X"], L["W"]
     A, B = H.upload(nv, a), H.upload(nv, b)
-    D = nv.nvfp4_gemm(A, B, tile=nv.TILE_PAIR_256X256)
+    ref = orc.gemm_fp64(a, b)
+    D = nv.nvfp4_gemm(A, B, tile=tile)
+    H.assert_gemm_close(H.host_f64(D), ref, f"bf16 tile {tile}")
     rng = np.random.Generator(np.random.PCG64(5))
     W0 = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).cuda()
     acc = W0.clone()
-    nv.nvfp4_gemm(A, B, out=acc, d_mode=nv.D_F32_ACCUM, tile=nv.TILE_PAIR_256X256)
+    nv.nvfp4_gemm(A, B, out=acc, d_mode=nv.D_F32_ACCUM, tile=tile)
     assert torch.equal(acc, W0 + D.float())
     Cb = H.dev_bf16(syn.gradients((M, N), seed=9))
-    E = nv.nvfp4_gemm(A, B, d_mode=nv.D_BF16_ADD_C, C_add=Cb, tile=nv.TILE_PAIR_256X256)
-    H.assert_gemm_close(H.host_f64(E), orc.gemm_fp64(a, b) + H.host_f64(Cb), "ADD_C pair")
+    if tile == nv.TILE_PAIR_256X384:
+        with pytest.raises(nv.NVFP4Error) as e:
+            nv.nvfp4_gemm(A, B, d_mode=nv.D_BF16_ADD_C, C_add=Cb, tile=tile)
+        assert e.value.status == nv.ERR_INVALID_ARG
+    else:
+        E = nv.nvfp4_gemm(A, B, d_mode=nv.D_BF16_ADD_C, C_add=Cb, tile=tile)
+        H.assert_gemm_close(H.host_f64(E), ref + H.host_f64(Cb), "ADD_C pair")
     nv.check_device_errors()
+
+
+def test_gemm_wide_pair_tile_equals_pair_tile_llama8b(nv):
+    """The 384-wide pair tile (two MMAs per K step, N = 256 and N = 128, two
+    tensor-memory scale slots) against the 256-wide one at the bench's full
+    shapes (M=8192, K=4096, N=14336: FPROP, DGRAD through W's transposed
+    view, WGRAD of the column operands) on GPU-quantised operands: every
+    output element identical (the same MMAs accumulate each element in the
+    same K order), in the bf16 and the FP32-fold modes."""
+    import torch
+    M, K, N = 8192, 4096, 14336
+    X, W, dY = syn.linear_layer(M, K, N)
+    qX = nv.nvfp4_quantize(H.dev_bf16(X), nv.ROW_1X16)
+    qW = nv.nvfp4_quantize(H.dev_bf16(W), nv.BLOCK_16X16, nv.EMIT_T)
+    qdY = nv.nvfp4_quantize(H.dev_bf16(dY), nv.ROW_1X16, nv.SR, seed=0, offset=0)
+    qdYc = nv.nvfp4_quantize(H.dev_bf16(dY), nv.COL_1X16, nv.RHT | nv.SR, seed=0, offset=1)
+    qXc = nv.nvfp4_quantize(H.dev_bf16(X), nv.COL_1X16, nv.RHT, seed=0)
+    for name, a, b, bv in (("FPROP", qX, qW, 0), ("DGRAD", qdY, qW, 1), ("WGRAD", qdYc, qXc, 0)):
+        d3 = nv.nvfp4_gemm(a, b, b_view=bv, tile=nv.TILE_PAIR_256X256)
+        d6 = nv.nvfp4_gemm(a, b, b_view=bv, tile=nv.TILE_PAIR_256X384)
+        nv.check_device_errors()
+        assert torch.equal(d3, d6), f"{name}: 384-wide tile differs from the 256-wide tile"
+        del d3, d6
+    acc3 = torch.full((M, N), 0.25, dtype=torch.float32, device="cuda")
+    acc6 = acc3.clone()
+    nv.nvfp4_gemm(qX, qW, out=acc3, d_mode=nv.D_F32_ACCUM, tile=nv.TILE_PAIR_256X256)
+    nv.nvfp4_gemm(qX, qW, out=acc6, d_mode=nv.D_F32_ACCUM, tile=nv.TILE_PAIR_256X384)
+    nv.check_device_errors()
+    assert torch.equal(acc3, acc6)
 
 
 def test_gemm_end_to_end_gpu_quantiser(nv, orc):
