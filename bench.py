@@ -35,11 +35,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roofline"
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
-# DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM at
-# M=8192, N=14336, K=4096, from one ncu capture of that launch
-# (dram__bytes_read.sum 55.5 MB + dram__bytes_write.sum 187.9 MB); None once
-# the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = None  # dram read + write, one FPROP launch
+# DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM
+# (256 x 384 tiles) at M=8192, N=14336, K=4096, from one ncu capture of that
+# launch (dram__bytes_read.sum 55.5 MB + dram__bytes_write.sum 187.7 MB); None
+# once the kernel changes after the capture.
+FPROP_TRAFFIC_BYTES = 55.467776e6 + 187.748096e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 # Warp instructions one launch of dY's one-read quantiser (row SR + column
 # RHT + SR, quant_rowcol_kernel<1, 1, 1>) executes at dY [8192, 14336], from
