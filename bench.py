@@ -47,7 +47,7 @@ FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 # changes after the capture.  The kernel is bound by instruction issue, not
 # by HBM: its roofline is the issue rate of 4 schedulers per SM, one warp
 # instruction each per cycle.
-SR_ROWCOL_INSTRUCTIONS = 361444303
+SR_ROWCOL_INSTRUCTIONS = None
 SR_ROWCOL_SHAPE = (8192, 14336)  # (M, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "

@@ -98,6 +98,24 @@ NVFP4_DEV uint8_t* align_smem_1024(uint8_t* raw) {
   return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
 }
 
+// Tile row and column (tile = tr * ntc + tc) of a CTA's tiles, which step by
+// the grid size: advanced by an add and a carry per tile instead of a 64-bit
+// division and remainder.  32-bit: the launchers refuse more than 2^30 tiles
+// (a tile is 8192 elements, so no tensor that fits in memory has as many).
+struct TileWalk {
+  int32_t tr, tc, dr, dc, ntc;
+  NVFP4_DEV TileWalk(int32_t tile0, int32_t step, int32_t n)
+      : tr(tile0 / n), tc(tile0 % n), dr(step / n), dc(step % n), ntc(n) {}
+  NVFP4_DEV void next() {
+    tc += dc;
+    tr += dr;
+    if (tc >= ntc) {
+      tc -= ntc;
+      ++tr;
+    }
+  }
+};
+
 // Byte offset of (row r, byte b of the tile row) inside a stage.
 template <class G>
 NVFP4_DEV uint32_t swz(int r, int b) {
@@ -307,13 +325,14 @@ NVFP4_DEV void q_produce(const CUtensorMap* tm, uint32_t stage0, uint32_t bar_fu
                          uint32_t bar_empty, volatile int* abort_flag, int64_t ntiles,
                          int64_t ntc) {
   prefetch_tmap(tm);
-  int64_t k = 0;
+  uint32_t k = 0;
   if (*reinterpret_cast<volatile unsigned int*>(&g_q_stall)) return;  // injected: no loads
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+  TileWalk tw((int32_t)blockIdx.x, (int32_t)gridDim.x, (int32_t)ntc);
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k, tw.next()) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_empty + 8 * s, (uint32_t)((k / G::kStages) & 1) ^ 1u, abort_flag, 0x40u))
       break;
-    const int32_t x = (int32_t)((tile % ntc) * G::kTC), y = (int32_t)((tile / ntc) * G::kTR);
+    const int32_t x = (int32_t)(tw.tc * G::kTC), y = (int32_t)(tw.tr * G::kTR);
     mbar_arrive_expect_tx(bar_full + 8 * s, G::kStageBytes);
 #pragma unroll
     for (int b = 0; b < G::kNBox; ++b)
@@ -360,8 +379,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int64_t apr = ((C / 16) + 3) / 4;
   const uint32_t sign_bits = RHT ? rht_sign_bits(p.seed) : 0u;
   uint8_t* wat = smem + L::offExtra + warp * 64;
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+  uint32_t k = 0;
+  TileWalk tw((int32_t)blockIdx.x, (int32_t)gridDim.x, (int32_t)ntc);
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k, tw.next()) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
     const uint8_t* st = smem + s * G::kStageBytes;
@@ -372,7 +392,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
 
-    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t tr = tw.tr, tc = tw.tc;
     const int64_t c0 = tc * G::kTC + c8 * 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -474,8 +494,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int64_t apr = ((R / 16) + 3) / 4;
   uint32_t smask[16] = {};  // the transform's sign of block row e (bit 31)
   if (RHT) rht_sign_masks(rht_sign_bits(p.seed), smask);
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+  uint32_t k = 0;
+  TileWalk tw((int32_t)blockIdx.x, (int32_t)gridDim.x, (int32_t)ntc);
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k, tw.next()) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
     const uint8_t* st = smem + s * G::kStageBytes;
@@ -489,7 +510,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
 
-    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t tr = tw.tr, tc = tw.tc;
     const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
     const int buf = (int)(k & 1);
     uint32_t* out_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + buf * kBuf);
@@ -591,8 +612,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int64_t pc4_r = ((C / 16) + 3) / 4 * 4;  // padded scale columns of the row operand
   uint32_t smask[16] = {};  // the transform's sign of block row e (bit 31)
   if (RHT) rht_sign_masks(rht_sign_bits(p.seed), smask);
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+  uint32_t k = 0;
+  TileWalk tw((int32_t)blockIdx.x, (int32_t)gridDim.x, (int32_t)ntc);
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k, tw.next()) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
     const uint8_t* st = smem + s * G::kStageBytes;
@@ -605,7 +627,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
       vb[e] = f.y;
     }
 
-    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t tr = tw.tr, tc = tw.tc;
     const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
     // ---- column operand: staged for the coalesced stores below
     const int buf = (int)(k & 1);
@@ -727,8 +749,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int64_t apr_t = ((R / 16) + 3) / 4;  // transposed view
   uint32_t* ok_s = reinterpret_cast<uint32_t*>(smem + L::offExtra + warp * kWarpBytes);
   uint8_t* ot_s = smem + L::offExtra + warp * kWarpBytes + kWarpK;
-  int64_t k = 0;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+  uint32_t k = 0;
+  TileWalk tw((int32_t)blockIdx.x, (int32_t)gridDim.x, (int32_t)ntc);
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k, tw.next()) {
     const int s = (int)(k % G::kStages);
     if (!q_wait(bar_full + 8 * s, (uint32_t)((k / G::kStages) & 1), abort_flag, 0x41u)) break;
     const uint8_t* st = smem + s * G::kStageBytes;
@@ -739,7 +762,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
 
-    const int64_t tr = tile / ntc, tc = tile % ntc;
+    const int64_t tr = tw.tr, tc = tw.tc;
     const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
     const int64_t r = r0 + rl;
     const bool row_ok = r0 + 16 * warp < R;  // rows come in whole 16-row strips
@@ -1008,6 +1031,7 @@ template <auto KERN, class L>
 nvfp4_status launch_q(const CUtensorMap& tm, const QParams& p, int64_t ntiles, int sms,
                       cudaStream_t s) {
   static LaunchState ls;
+  if (ntiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;  // the kernels' 32-bit tile walk
   const int per_sm = resident_per_sm(ls, KERN, kQThreads, L::kAlloc);
   if (per_sm <= 0) return NVFP4_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
@@ -1109,6 +1133,7 @@ template <auto KERN>
 nvfp4_status launch_rowcol(const CUtensorMap& tm, const QRowColParams& p, int64_t ntiles, int sms,
                            cudaStream_t s) {
   static LaunchState ls;
+  if (ntiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;  // the kernels' 32-bit tile walk
   const int per_sm = resident_per_sm(ls, KERN, kQThreads, RowColL::kAlloc);
   if (per_sm <= 0) return NVFP4_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
