@@ -265,6 +265,20 @@ NVFP4_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_
 NVFP4_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization (launch_pdl) may be scheduled while the kernel before it on
+// the stream is still finishing, so it runs its on-chip setup (barriers,
+// tensor memory, tables) early and waits here -- for that kernel to complete
+// and its writes to be visible -- before it reads or writes global memory.
+// Returns at once in a kernel launched without the attribute.  Then lets the
+// next kernel on the stream be scheduled (its CTAs take whatever room this
+// grid leaves and wait in their own griddep_wait): every CTA of this grid is
+// resident and running by the time all of them have passed this point.
+NVFP4_DEV void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 NVFP4_DEV void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -629,6 +630,7 @@ __launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();
 
   if (warp < R::kEpi0) {
   // issue warps (the register hint sits inside the branch so that the code it
@@ -1039,6 +1041,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair384Smem::kThread
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();
 
   if (warp < 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kRegsIssue));
@@ -1359,8 +1362,10 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   }
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
-  kern<<<grid, R::kThreads, L::kAlloc, stream>>>(ma, mb, msa, msb, md, a);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(kern, grid, R::kThreads, L::kAlloc, stream, ma, mb, msa, msb, md, a) ==
+                 cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
 }
 
 
@@ -1402,8 +1407,10 @@ nvfp4_status launch_pair384(const CUtensorMap& ma, const CUtensorMap& mb, const 
   }
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
-  kern<<<grid, L::kThreads, L::kAlloc, stream>>>(ma, mb, mb2, msa, msb, md, a);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(kern, grid, L::kThreads, L::kAlloc, stream, ma, mb, mb2, msa, msb, md, a) ==
+                 cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
 }
 
 template <int BN, int STAGES, int DMODE, int BKB>
@@ -1421,8 +1428,10 @@ nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs
   // persistent grid: one CTA per SM (tensor memory and shared memory admit
   // one), at most one per output tile
   const int units = a.num_m_blk * a.num_n_blk;
-  kern<<<std::min(units, sms), kThreads, L::kAlloc, stream>>>(ma, mb, a);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(kern, std::min(units, sms), kThreads, L::kAlloc, stream, ma, mb, a) ==
+                 cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
 }
 
 template <int BN, int STAGES, int BKB>

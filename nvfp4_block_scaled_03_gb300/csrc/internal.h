@@ -11,6 +11,27 @@
 
 namespace nvfp4 {
 
+// Launches kern with programmatic stream serialization: the grid may be
+// scheduled before the previous kernel on the stream has finished, and each
+// kernel launched this way calls griddep_wait() before its first access to
+// global memory.  Within a captured CUDA graph the same dependency becomes a
+// programmatic edge.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct DeviceInfo {
   int device;
   int sm_count;

@@ -366,6 +366,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
   float* tab = reinterpret_cast<float*>(smem + L::offTab);
   q_init<G, L>(smem);
+  griddep_wait();
   const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
   fill_enc_table(tab, s_enc);  // ends with a CTA barrier
 
@@ -481,6 +482,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
   float* tab = reinterpret_cast<float*>(smem + L::offTab);
   q_init<G, L>(smem);
+  griddep_wait();
   const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
   fill_enc_table(tab, s_enc);
 
@@ -591,6 +593,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
   float* tab_c = reinterpret_cast<float*>(smem + L::offTab);
   float* tab_r = reinterpret_cast<float*>(smem + L::offExtra + 2 * kBuf);
   q_init<G, L>(smem);
+  griddep_wait();
   const float s_enc_r = per_tensor_s_enc(*p.row_amax), s_enc_c = per_tensor_s_enc(*p.col_amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *p.row_s_dec = __fdiv_rn(1.0f, s_enc_r);
@@ -734,6 +737,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc);
   float* tab = reinterpret_cast<float*>(smem + L::offTab);
   q_init<G, L>(smem);
+  griddep_wait();
   const float s_enc = tensor_s_enc(p, reinterpret_cast<float*>(smem + L::offRed));
   fill_enc_table(tab, s_enc);
 
@@ -868,6 +872,7 @@ template <typename T>
 __global__ void __launch_bounds__(kAmaxThreads) amax_plain_kernel(const QParams p) {
   constexpr int kU = 8;
   __shared__ float red[kAmaxThreads / 32];
+  griddep_wait();
   const T* x = static_cast<const T*>(p.x);
   const int64_t C = p.cols, ld = p.ld, cpr = C / 8, n = p.rows * cpr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -907,6 +912,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_col_kernel(const QParam
   const T* x = static_cast<const T*>(p.x);
   const int64_t ld = p.ld, cpr = p.cols / kCh, n = (p.rows / 16) * cpr;
   const uint32_t sign_bits = rht_sign_bits(p.seed);
+  griddep_wait();
   float m = 0.0f;
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -961,6 +967,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_finalize_kernel(const float
                                                                      int n, float* out0,
                                                                      float* out1) {
   __shared__ float red[kAmaxThreads / 32];
+  griddep_wait();
   float m0 = 0.0f, m1 = 0.0f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     m0 = fmaxf(m0, partials[i]);
@@ -982,6 +989,7 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_rht_row_kernel(const QParam
   const T* x = static_cast<const T*>(p.x);
   const int64_t bpr = p.cols / 16, n = p.rows * bpr;
   const uint32_t sign_bits = rht_sign_bits(p.seed);
+  griddep_wait();
   float m = 0.0f;
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -1035,14 +1043,13 @@ nvfp4_status launch_q(const CUtensorMap& tm, const QParams& p, int64_t ntiles, i
   const int per_sm = resident_per_sm(ls, KERN, kQThreads, L::kAlloc);
   if (per_sm <= 0) return NVFP4_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
-  KERN<<<grid, kQThreads, L::kAlloc, s>>>(tm, p);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(KERN, grid, kQThreads, L::kAlloc, s, tm, p) == cudaSuccess ? NVFP4_OK
+                                                                       : NVFP4_ERR_CUDA;
 }
 
 template <auto KERN>
 nvfp4_status launch_amax_kernel(const QParams& p, int grid, cudaStream_t s) {
-  KERN<<<grid, kAmaxThreads, 0, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(KERN, grid, kAmaxThreads, 0, s, p) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 // Grid of an amax kernel: as many CTAs as are resident at once, at most 4 per
@@ -1137,8 +1144,9 @@ nvfp4_status launch_rowcol(const CUtensorMap& tm, const QRowColParams& p, int64_
   const int per_sm = resident_per_sm(ls, KERN, kQThreads, RowColL::kAlloc);
   if (per_sm <= 0) return NVFP4_ERR_CUDA;
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
-  KERN<<<grid, kQThreads, RowColL::kAlloc, s>>>(tm, p);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(KERN, grid, kQThreads, RowColL::kAlloc, s, tm, p) == cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
 }
 
 }  // namespace
@@ -1263,8 +1271,10 @@ nvfp4_status amax_impl(const void* x, int32_t in_dtype, int64_t rows, int64_t co
   if (st != NVFP4_OK) return st;
   float* out0 = amax_rht ? amax_rht : amax_plain;
   float* out1 = amax_rht ? amax_plain : nullptr;
-  amax_finalize_kernel<<<1, kAmaxThreads, 0, stream>>>(p.partials, grid, out0, out1);
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return launch_pdl(amax_finalize_kernel, 1, kAmaxThreads, 0, stream,
+                    static_cast<const float*>(p.partials), grid, out0, out1) == cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
 }
 
 nvfp4_status quant_set_injection(unsigned int stall, unsigned long long wait_ns) {
