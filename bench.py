@@ -37,9 +37,9 @@ METRIC = "NVFP4 MLP GEMM TFLOP/s and quantize GB/s on 1 GB300, % of FP4/HBM roof
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense-rate ratio (6x)
 # DRAM bytes (read + write) of one FPROP launch of the CTA-pair GEMM
 # (256 x 384 tiles) at M=8192, N=14336, K=4096, from one ncu capture of that
-# launch (dram__bytes_read.sum 55.5 MB + dram__bytes_write.sum 187.7 MB); None
+# launch (dram__bytes_read.sum 56.1 MB + dram__bytes_write.sum 187.4 MB); None
 # once the kernel changes after the capture.
-FPROP_TRAFFIC_BYTES = 55.467776e6 + 187.748096e6  # dram read + write, one FPROP launch
+FPROP_TRAFFIC_BYTES = 56.074240e6 + 187.385344e6  # dram read + write, one FPROP launch
 FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 # Warp instructions one launch of dY's one-read quantiser (row SR + column
 # RHT + SR, quant_rowcol_kernel<1, 1, 1>) executes at dY [8192, 14336], from
@@ -47,7 +47,7 @@ FPROP_TRAFFIC_SHAPE = (8192, 4096, 14336)  # (M, K, N) the capture was taken at
 # changes after the capture.  The kernel is bound by instruction issue, not
 # by HBM: its roofline is the issue rate of 4 schedulers per SM, one warp
 # instruction each per cycle.
-SR_ROWCOL_INSTRUCTIONS = None
+SR_ROWCOL_INSTRUCTIONS = 303759452
 SR_ROWCOL_SHAPE = (8192, 14336)  # (M, N) the capture was taken at
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DATA = ("synthetic, seeded PCG64: X ~ N(0,1) with x50 outliers at rate 1e-3, W ~ N(0,0.02), "
