@@ -771,33 +771,48 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const int64_t r = r0 + rl;
     const bool row_ok = r0 + 16 * warp < R;  // rows come in whole 16-row strips
     const int64_t g = tr * 8 + warp;         // 16-row block: scale column of the transposed view
-    uint32_t scw = 0;
+    // the four 16x16 blocks side by side, one step at a time, so that their
+    // warp reductions, table reads and shuffles are in flight together
+    uint32_t scw = 0, sc[4], packed[4];
+    float mb[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const bool ok = row_ok && (c0 + 16 * b < C);
       float m = 0.0f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[b][e]));
-      // the 16x16 block's maximum in one warp reduction: non-negative floats
-      // order like their bit patterns read as unsigned integers
-      m = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
-      const uint32_t sc = ok ? block_scale_code(m, s_enc) : 0u;
-      const float enc = encode_factor(tab, sc);
+      mb[b] = m;
+    }
+    // each block's maximum in one warp reduction: non-negative floats order
+    // like their bit patterns read as unsigned integers
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      mb[b] = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mb[b])));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const bool ok = row_ok && (c0 + 16 * b < C);
+      sc[b] = ok ? block_scale_code(mb[b], s_enc) : 0u;
+      const float enc = encode_factor(tab, sc[b]);
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
       if (SR && ok) {
         const uint64_t idx = (uint64_t)(r * C + c0 + 16 * b + 8 * h);
         w0 = sr_words(p.rk, p.offset, idx);
         w1 = sr_words(p.rk, p.offset, idx + 4);
       }
-      const uint32_t packed = encode8<SR>(v[b], enc, w0, w1);
-      ok_s[rl16 * kKWords + 2 * b + h] = packed;
-      scw |= sc << (8 * b);
-      if (EMIT_T) {
+      packed[b] = encode8<SR>(v[b], enc, w0, w1);
+      ok_s[rl16 * kKWords + 2 * b + h] = packed[b];
+      scw |= sc[b] << (8 * b);
+    }
+    if (EMIT_T) {
+      uint32_t others[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) others[b] = __shfl_xor_sync(0xFFFFFFFFu, packed[b], 1);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
         // transposed byte of column e = code(even row, e) | code(odd row, e) << 4:
         // t holds columns 0, 2, 4, 6 and u columns 1, 3, 5, 7 of the lane
         // pair's 8 columns; the even lane stores columns 0-3, the odd 4-7
-        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, packed, 1);  // row rl ^ 1
-        const uint32_t lo = (lane & 1) ? other : packed, hi = (lane & 1) ? packed : other;
+        const uint32_t other = others[b];  // row rl ^ 1
+        const uint32_t lo = (lane & 1) ? other : packed[b], hi = (lane & 1) ? packed[b] : other;
         const uint32_t t = (lo & 0x0F0F0F0Fu) | ((hi & 0x0F0F0F0Fu) << 4);
         const uint32_t u = ((lo >> 4) & 0x0F0F0F0Fu) | (hi & 0xF0F0F0F0u);
         const uint32_t w = (lane & 1) ? __byte_perm(t, u, 0x7362) : __byte_perm(t, u, 0x5140);
@@ -808,7 +823,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
         if (lane < 16 && g < 4 * apr_t) {
           const int64_t orow = c0 + 16 * b + lane;
           p.scales_t[((orow >> 7) * apr_t + (g >> 2)) * 512 + (orow & 31) * 16 +
-                     ((orow >> 5) & 3) * 4 + (g & 3)] = (uint8_t)sc;
+                     ((orow >> 5) & 3) * 4 + (g & 3)] = (uint8_t)sc[b];
         }
       }
     }
