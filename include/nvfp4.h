@@ -14,7 +14,13 @@
  *    frees or synchronises on the hot path (nvfp4_check_device_errors is the
  *    one call that synchronises).
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
- *    the legacy default stream).
+ *    the legacy default stream).  Nothing on the hot path allocates or
+ *    synchronises, so a sequence of calls can be captured into a CUDA graph
+ *    and replayed (after one uncaptured call of each, which configures the
+ *    kernels).  The quantiser, amax and GEMM kernels are launched with
+ *    programmatic stream serialization: a kernel may be scheduled while the
+ *    previous one on the stream finishes, and waits for it to complete before
+ *    it touches global memory, so stream order is kept.
  *  - Argument errors are reported by the return value before anything is
  *    launched; a failed launch returns NVFP4_ERR_CUDA.  Device-side wait
  *    timeouts (a hung pipeline) are recorded in a device error word and
