@@ -119,9 +119,8 @@ nvfp4_status nvfp4_check_device_errors(nvfp4_stream stream);
  * in flight when the kernel gives up, and it returns after recording the
  * timeout (nvfp4_check_device_errors then reports NVFP4_ERR_DEVICE_TIMEOUT):
  *   NVFP4_STALL_QUANTIZE  the quantise passes of nvfp4_quantize
- *   NVFP4_STALL_GEMM      the single-SM GEMM kernel (NVFP4_TILE_128X128 /
- *                         128X256 / 128X256_K128; the CTA-pair kernel is
- *                         not affected)
+ *   NVFP4_STALL_GEMM      every GEMM kernel (single-SM and CTA-pair tiles;
+ *                         on a pair a timeout in either CTA stops both)
  * wait_limit_ns sets how long those kernels' pipeline waits last before they
  * give up (0: the default, 2 s); the waits that drain copies and MMAs
  * already issued keep their own 2 s limit.  Synchronises the device, then

@@ -29,9 +29,9 @@
 namespace nvfp4 {
 
 static __device__ unsigned int g_gemm_error;
-// Failure injection for tests of the bounded waits (nvfp4_debug_inject),
-// single-SM kernel only: while g_gemm_stall is set its producer issues no
-// loads, and its pipeline waits give up after g_gemm_wait_ns.
+// Failure injection for tests of the bounded waits (nvfp4_debug_inject):
+// while g_gemm_stall is set the producers of every GEMM kernel issue no
+// loads, and the pipeline waits give up after g_gemm_wait_ns.
 static __device__ unsigned int g_gemm_stall;
 static __device__ unsigned long long g_gemm_wait_ns = 2000000000ull;
 
@@ -561,10 +561,11 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
                                  uint32_t peer_abort_addr, unsigned int code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = *reinterpret_cast<volatile unsigned long long*>(&g_gemm_wait_ns);
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       st_cluster_u32(peer_abort_addr, 1u);
       atomicCAS(&g_gemm_error, 0u, code);
@@ -644,7 +645,8 @@ __launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
       prefetch_tmap(&tmSFA);
       prefetch_tmap(&tmSFB);
       uint32_t s = 0, ph = 0;
-      bool ok = true;
+      // injected stall: no loads, so every consumer's first wait runs out
+      bool ok = *reinterpret_cast<volatile unsigned int*>(&g_gemm_stall) == 0u;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
         const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
         const int a_rb = m_blk * 2 + (int)rank;  // this CTA's 128-row block of A
@@ -1054,7 +1056,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair384Smem::kThread
       prefetch_tmap(&tmSFA);
       prefetch_tmap(&tmSFB);
       uint32_t s = 0, ph = 0;
-      bool ok = true;
+      // injected stall: no loads, so every consumer's first wait runs out
+      bool ok = *reinterpret_cast<volatile unsigned int*>(&g_gemm_stall) == 0u;
       for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
         const int m_blk = tile % args.num_m_blk, n_blk = tile / args.num_m_blk;
         const int a_rb = m_blk * 2 + (int)rank;  // this CTA's 128-row block of A

@@ -48,7 +48,7 @@ def test_quantize_wait_expires_then_recovers(nv, orc, mode, flags):
     H.assert_quant_equal(q, orc.quantize(x, mode, flags, seed=3, offset=1), "after recovery")
 
 
-@pytest.mark.parametrize("tile", [1, 2, 5])
+@pytest.mark.parametrize("tile", [1, 2, 5, 3, 6])  # single-SM tiles, then the CTA pairs
 def test_gemm_wait_expires_then_recovers(nv, orc, tile):
     X, W = syn.activations((128, 512), seed=1), syn.weights((256, 512), seed=2)
     a, b = orc.quantize(X, orc.ROW_1X16), orc.quantize(W, orc.BLOCK_16X16)
