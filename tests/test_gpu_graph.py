@@ -98,3 +98,44 @@ def test_layer_step_graph_replay_equals_eager(nv):
         for k, v in eager.items():
             assert torch.equal(v.view(torch.uint8), now[k].view(torch.uint8)), \
                 f"replay {replay}: {k} differs from the eager step"
+
+
+def test_mlp_step_graph_replay_equals_eager(nv):
+    """The SwiGLU MLP forward + backward (nine GEMMs, the SwiGLU kernels,
+    every quantisation of the recipe, WGRAD folded into FP32 master
+    gradients) captured as one graph: a replay writes Y, dX and the folded
+    gradients exactly as the eager calls do."""
+    import torch
+    M, D, F = 512, 512, 1024
+    g = torch.Generator(device="cuda").manual_seed(11)
+    X = torch.randn(M, D, generator=g, device="cuda").to(torch.bfloat16)
+    dY = (1e-3 * torch.randn(M, D, generator=g, device="cuda")).to(torch.bfloat16)
+    Wg, Wu = (0.02 * torch.randn(F, D, generator=g, device="cuda") for _ in range(2))
+    Wd = 0.02 * torch.randn(D, F, generator=g, device="cuda")
+    sb, wb = nv.mlp_sizes(M, D, F)
+    saved = torch.empty(sb, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    Y = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+    dX = torch.empty_like(Y)
+    grads = [torch.zeros_like(w) for w in (Wg, Wu, Wd)]
+    p = nv.mlp_params(M, D, F, Wg, Wu, Wd, seed=5, step=3, rht=True)
+
+    def step():
+        for t in grads:
+            t.zero_()
+        nv.nvfp4_mlp_fwd(p, X, Y, saved, ws)
+        nv.nvfp4_mlp_bwd(p, dY, saved, dX, *grads, ws)
+
+    step()
+    nv.check_device_errors()
+    eager = [t.clone() for t in (Y, dX, *grads)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for t in (Y, dX, *grads):
+        t.fill_(0)
+    graph.replay()
+    torch.cuda.synchronize()
+    nv.check_device_errors()
+    for name, a, b in zip(("Y", "dX", "dWg", "dWu", "dWd"), eager, (Y, dX, *grads)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"{name} differs"
