@@ -520,15 +520,17 @@ NVFP4_DEV void tc_mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, u
 
 template <int STAGES, int FMT, bool IMG>
 struct PairSmem {
-  static constexpr bool kST = FMT == kFmtNVF4 && !IMG;  // scales through tcgen05.st
+  // NVFP4 stores its scales into tensor memory from the scale warps; the MX
+  // formats copy them (IMG: B's scales as images)
+  static_assert(IMG == (FMT != kFmtNVF4), "scale path of the format");
+  static constexpr bool kST = !IMG;  // scales through tcgen05.st
   static constexpr int kAt = PairFmt<FMT>::kAtoms;
   static constexpr uint32_t kA = 128 * kBKBytes;               // this CTA's 128 A rows
   static constexpr uint32_t kB = 128 * kBKBytes;               // this CTA's 128 B rows
   // B's scales either as the plain atoms of the tile's two 128-row blocks
-  // (two 32x128b.warpx4 copies per K step), or as 4 KB images, one per scale
-  // atom along K (the two row halves' atoms, each repeated for the four
-  // 32-lane quarters), that one 128-lane x 256-bit copy each moves into
-  // tensor memory
+  // (stored), or as 4 KB images, one per scale atom along K (the two row
+  // halves' atoms, each repeated for the four 32-lane quarters), that one
+  // 128-lane x 256-bit copy each moves into tensor memory
   static constexpr uint32_t kSFA = kAt * 512;                  // own A rows' scale atoms
   static constexpr uint32_t kSFB = IMG ? kAt * 4096 : kAt * 1024;
   // bytes counted on the leader's full barrier: both CTAs' A and B, and with
@@ -576,7 +578,7 @@ NVFP4_DEV bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile int* ab
 
 template <int STAGES, int DMODE, int FMT, bool IMG>
 __global__ void __cluster_dims__(2, 1, 1)
-__launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
+__launch_bounds__(PairRoles<!IMG>::kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA,
@@ -674,17 +676,10 @@ __launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
             if (++s == STAGES) { s = 0; ph ^= 1u; }
             continue;
           }
-          // scale atoms as 128-byte rows (4 per atom)
+          // A's scale atoms as 128-byte rows (4 per atom), B's as images
           tma_load_2d_pair(sbase + L::offSFA + s * L::kSFA, &tmSFA, fb, 0,
                            (a_rb * args.kg + kb * kAt) * 4);
-          if (IMG) {
-            tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
-          } else {  // the two row blocks' atoms (a block past N reads as zeros)
-            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, 0,
-                             (b_rb0 * args.kg + kb * kAt) * 4);
-            tma_load_2d_pair(sbase + L::offSFB + s * L::kSFB + kAt * 512, &tmSFB, fb, 0,
-                             ((b_rb0 + 1) * args.kg + kb * kAt) * 4);
-          }
+          tma_load_5d_pair(sbase + L::offSFB + s * L::kSFB, &tmSFB, fb, b_rb0, kb * kAt);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -771,14 +766,8 @@ __launch_bounds__(PairRoles<FMT == kFmtNVF4 && !IMG>::kThreads, 1)
           for (int j = 0; j < natoms; ++j) {
             if (j % kPairCopyWarps == cw)
               tc_cp_pair_32x128b_warpx4(sfa_t + 4 * j, smem_desc_sf(sa + j * 512));
-            if ((kAt + j) % kPairCopyWarps == cw) {
-              if (IMG) {
-                tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
-              } else {
-                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j, smem_desc_sf(sb + j * 512));
-                tc_cp_pair_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc_sf(sb + (kAt + j) * 512));
-              }
-            }
+            if ((kAt + j) % kPairCopyWarps == cw)
+              tc_cp_pair_128x256b(sfb_t + 8 * j, smem_desc_sf_image(sb + j * 4096));
           }
           issued = true;
           // the MMA thread may issue as soon as these copies are issued: the
