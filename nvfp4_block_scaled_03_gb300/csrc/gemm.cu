@@ -1310,6 +1310,58 @@ bool make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per-device, once-per-kernel launch set-up of a GEMM kernel, under a lock:
+// its dynamic shared memory attribute, for a kernel that splits registers
+// with setmaxnreg the check that the compiled count covers the split
+// (setmaxnreg.inc waits until the registers it asks for are free in the
+// block's launch allotment, so a split above it would wait forever), and
+// for a CTA-pair kernel how many pairs are resident at once (cluster
+// placement can leave SMs of a GPC unpaired).  Returns the resident pairs
+// (1 for a single-SM kernel), 0 when the set-up failed.
+struct GemmLaunchState {
+  std::mutex mu;
+  int resident[64] = {};  // per device: 0 not yet set up, -1 refused for good
+};
+
+template <typename K>
+int gemm_setup(GemmLaunchState& ls, K kern, uint32_t smem, int threads, int split_regs,
+               bool pair, int sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(ls.mu);
+  if (ls.resident[dev] == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return 0;
+    if (split_regs > 0) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return 0;
+      if (fa.numRegs * threads < split_regs) {
+        ls.resident[dev] = -1;  // this build can never run the kernel
+        return 0;
+      }
+    }
+    int n = 1;
+    if (pair) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (sms / 2));
+      cfg.blockDim = dim3(threads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+      n = std::min(n, sms / 2);
+    }
+    ls.resident[dev] = n;
+  }
+  return ls.resident[dev] > 0 ? ls.resident[dev] : 0;
+}
+
 template <int STAGES, int DMODE, int FMT, bool IMG>
 nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa,
                          const CUtensorMap& msb, const CUtensorMap& md, const GemmArgs& a, int sms,
@@ -1317,41 +1369,11 @@ nvfp4_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   using L = PairSmem<STAGES, FMT, IMG>;
   auto kern = gemm_nvf4_pair_kernel<STAGES, DMODE, FMT, IMG>;
   using R = PairRoles<L::kST>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
-        cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    if (L::kST) {
-      // setmaxnreg.inc waits until the registers it asks for are free in the
-      // block's launch allotment: refuse a build whose register count at
-      // launch cannot cover the split (it would wait forever)
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
-          fa.numRegs * R::kThreads < R::kSplitRegs)
-        return NVFP4_ERR_CUDA;
-    }
-    configured = true;
-  }
-  // persistent grid: as many pairs as can be resident at once (cluster
-  // placement can leave SMs of a GPC unpaired), at most one per tile
-  static int max_pairs = 0;
-  if (max_pairs == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(R::kThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
-    max_pairs = std::min(n, sms / 2);
-  }
+  static GemmLaunchState ls;
+  // persistent grid: as many pairs as are resident at once, at most one per tile
+  const int max_pairs =
+      gemm_setup(ls, kern, L::kAlloc, R::kThreads, L::kST ? R::kSplitRegs : 0, true, sms);
+  if (max_pairs <= 0) return NVFP4_ERR_CUDA;
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
   return launch_pdl(kern, grid, R::kThreads, L::kAlloc, stream, ma, mb, msa, msb, md, a) ==
@@ -1367,36 +1389,9 @@ nvfp4_status launch_pair384(const CUtensorMap& ma, const CUtensorMap& mb, const 
                             const GemmArgs& a, int sms, cudaStream_t stream) {
   using L = Pair384Smem;
   auto kern = gemm_nvf4_pair384_kernel<DMODE>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
-        cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    // setmaxnreg.inc waits until the registers it asks for are free in the
-    // block's launch allotment: refuse a build whose register count at launch
-    // cannot cover the split (it would wait forever)
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs * L::kThreads < L::kSplitRegs)
-      return NVFP4_ERR_CUDA;
-    configured = true;
-  }
-  static int max_pairs = 0;
-  if (max_pairs == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(L::kThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
-    max_pairs = std::min(n, sms / 2);
-  }
+  static GemmLaunchState ls;
+  const int max_pairs = gemm_setup(ls, kern, L::kAlloc, L::kThreads, L::kSplitRegs, true, sms);
+  if (max_pairs <= 0) return NVFP4_ERR_CUDA;
   const int tiles = a.num_m_blk * a.num_n_blk;
   const int grid = 2 * std::min(tiles, max_pairs);
   return launch_pdl(kern, grid, L::kThreads, L::kAlloc, stream, ma, mb, mb2, msa, msb, md, a) ==
@@ -1410,13 +1405,8 @@ nvfp4_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs
                     cudaStream_t stream) {
   using L = Smem<BN, STAGES, BKB>;
   auto kern = gemm_nvf4_kernel<BN, STAGES, DMODE, BKB>;
-  static bool configured = false;  // attribute is per function; setting it twice is harmless
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
-        cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    configured = true;
-  }
+  static GemmLaunchState ls;
+  if (gemm_setup(ls, kern, L::kAlloc, kThreads, 0, false, sms) <= 0) return NVFP4_ERR_CUDA;
   // persistent grid: one CTA per SM (tensor memory and shared memory admit
   // one), at most one per output tile
   const int units = a.num_m_blk * a.num_n_blk;
