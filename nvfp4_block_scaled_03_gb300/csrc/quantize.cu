@@ -629,6 +629,18 @@ __global__ void __launch_bounds__(kQThreads, 2)
       va[e] = f.x;
       vb[e] = f.y;
     }
+    // RNE forms: the row role's 32 values, still packed, are read now and the
+    // stage goes back to the producer before either role computes (the SR
+    // forms, short of registers, read them after the column role)
+    constexpr bool kEarly = !SRR && !SRC;
+    uint4 rw[4];
+    if constexpr (kEarly) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        rw[q] = *reinterpret_cast<const uint4*>(st + swz<G>(rr, (32 * bp + 8 * q) * 2));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
 
     const int64_t tr = tw.tr, tc = tw.tc;
     const int64_t r0 = tr * G::kTR, c0 = tc * G::kTC;
@@ -641,15 +653,26 @@ __global__ void __launch_bounds__(kQThreads, 2)
                         out_s, atom);
     col_block<RHT, SRC>(vb, 2 * cp + 1, j, rows_ok, c0, r0, R, C, s_enc_c, tab_c, p.rk,
                         p.col_offset, out_s, atom);
-    // ---- row operand: row r, columns cb .. cb + 31 (two blocks); its values
-    // are read from the stage after the column role's, then the stage is freed
+    // ---- row operand: row r, columns cb .. cb + 31 (two blocks)
     {
       float vr[4][8];
+      if constexpr (kEarly) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        lds8<G>(st, rr, 32 * bp + 8 * q, static_cast<const uint16_t*>(nullptr), vr[q]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t w[4] = {rw[q].x, rw[q].y, rw[q].z, rw[q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            vr[q][2 * i] = __uint_as_float(w[i] << 16);
+            vr[q][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          lds8<G>(st, rr, 32 * bp + 8 * q, static_cast<const uint16_t*>(nullptr), vr[q]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      }
       const int64_t r = r0 + rr, cb = c0 + 32 * bp;
       const bool row_ok = r < R;
       uint32_t words[4], scw = 0;
