@@ -692,10 +692,11 @@ __launch_bounds__(PairRoles<!IMG>::kThreads, 1)
   } else if (ST && warp >= 4) {
     // ------------------------------------------------------------ scale warps
     // Warp q (= warp % 4) stores each stage's 12 scale atoms into its 32-lane
-    // quarter of this CTA's tensor memory: lane i gets row i (16 bytes, 4
-    // columns) of A's atoms j (columns 4 j ..) and of B's atoms j of both
-    // row blocks (16 + 8 j .., 20 + 8 j ..) -- the layout the block-scaled
-    // MMA reads, which the four quarters all hold.  The stores are waited
+    // quarter of this CTA's tensor memory: lane i gets the 16-byte line i of
+    // an atom (the scale words of rows i, i + 32, i + 64, i + 96) in 4
+    // columns, for A's atoms j (columns 4 j ..) and B's atoms j of both row
+    // blocks (16 + 8 j .., 20 + 8 j ..) -- the layout the block-scaled MMA
+    // reads, which the four quarters all hold.  The stores are waited
     // for and fenced (tcgen05.fence::before_thread_sync) before the arrive;
     // the MMA thread's fence after its wait orders its MMAs behind them.
     const int q = warp & 3;
