@@ -13,8 +13,9 @@ Source of the method: the "NVFP4 pretraining recipe" page (re-post of NVIDIA's
 NVFP4 pretraining blog), sections "NVFP4 format and advantages" and "NVFP4
 pretraining recipe" (five bullets, Figure 1 text).  Every function here and
 in :mod:`oracle.mlp` is pinned by ``-m "not gpu"`` tests to something other
-than itself (brute force, closed forms, exhaustive searches, published
-generator outputs, invariants); none is left "parity unpinned".
+than itself (brute force, closed forms, exhaustive searches, another
+project's Philox4x32-10 run in its interpreter, invariants); none is left
+"parity unpinned".
 """
 from __future__ import annotations
 
