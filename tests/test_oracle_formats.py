@@ -35,6 +35,8 @@ def test_e4m3_points_match_golden(orc):
 def test_e4m3_saturation_and_subnormals(orc):
     assert orc.e4m3_rne_sat(448.0) == 0x7E
     assert orc.e4m3_rne_sat(464.0) == 0x7E      # halfway to 480: saturates
+    for t in (449.0, 470.0, 479.0, 480.0, 500.0):  # above the largest finite value
+        assert orc.e4m3_rne_sat(t) == 0x7E, t      # saturates, never the NaN code
     assert orc.e4m3_rne_sat(1e30) == 0x7E
     assert orc.e4m3_rne_sat(float("inf")) == 0x7E
     assert orc.e4m3_rne_sat(2.0 ** -9) == 0x01

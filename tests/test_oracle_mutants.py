@@ -1,0 +1,117 @@
+"""The oracle's pins catch plausible mistakes -- CPU only.
+
+Each case plants one mistake (a flipped tie rule, a wrong comparison, a
+dropped factor, a transposed index, a wrong constant) in a *copy* of the
+oracle's C source -- never in the oracle itself -- builds the copy as a
+separate package in a temporary directory and runs the pins that should
+notice it: at least one must fail.  The unmutated copy passes the same pins
+(the control), so a failure means the pin saw the mistake, not that the
+copy is broken.  (Saturating E4M3 only from 480 is no such case: the
+encoder's final clamp to 0x7E gives the same codes.)
+"""
+import importlib.util
+import os
+import shutil
+import sys
+
+import pytest
+
+import test_oracle_formats as formats
+import test_oracle_gemm as gemm
+import test_oracle_philox as philox
+import test_oracle_quantize as quantize
+import test_oracle_rht as rht
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# name -> (substitutions in nvfp4_oracle.c, pins that must catch it)
+MUTANTS = {
+    "E2M1 ties away from zero": (
+        [("else pick = ((lo & 1) == 0) ? lo : hi;", "else pick = hi;")],
+        [formats.test_e2m1_ties_to_even]),
+    "SR rounds up on r == threshold": (
+        [("int up = (double)rbits < thr;", "int up = (double)rbits <= thr;")],
+        [formats.test_e2m1_sr_rule]),
+    "E4M3 subnormal range ends at 2^-7": (
+        [("if (a < ldexp(1.0, -6)) {", "if (a < ldexp(1.0, -7)) {")],
+        [formats.test_e4m3_saturation_and_subnormals]),
+    "E4M3 subnormal step 2^-10": (
+        [("double n = rint(a * 512.0);", "double n = rint(a * 1024.0);")],
+        [formats.test_e4m3_saturation_and_subnormals]),
+    "RHT scaled by 1/2 instead of 1/4": (
+        [("for (int i = 0; i < 16; ++i) v[i] = v[i] * 0.25f;",
+          "for (int i = 0; i < 16; ++i) v[i] = v[i] * 0.5f;")],
+        [rht.test_butterfly_builds_the_sylvester_matrix,
+         rht.test_rht_cancels_in_the_wgrad_product]),
+    "RHT butterfly difference reversed": (
+        [("v[i + h] = a - b;", "v[i + h] = b - a;")],
+        [rht.test_butterfly_builds_the_sylvester_matrix]),
+    "Philox Weyl constant off by one": (
+        [("k1 += 0xBB67AE85u;", "k1 += 0xBB67AE86u;")],
+        [philox.test_philox_matches_triton_interpreter]),
+    "SR word taken from the neighbouring lane": (
+        [("return out[idx & 3];", "return out[(idx + 1) & 3];")],
+        [philox.test_sr_word_layout]),
+    "scale layout with row quarter and column swapped": (
+        [("return atom * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4);",
+          "return atom * 512 + (r % 32) * 16 + (c % 4) * 4 + ((r / 32) % 4);")],
+        [quantize.test_swizzle_matches_reshape_formulation]),
+    "nibbles packed high first": (
+        [("if ((j & 1) == 0) row[j / 2]", "if ((j & 1) == 1) row[j / 2]")],
+        [lambda o: quantize.test_row_quantize_brute_force(o, "bf16", (32, 64))]),
+    "zero tensor gets s_enc = 0": (
+        [("if (amax == 0.0f) return 1.0f;", "if (amax == 0.0f) return 0.0f;")],
+        [quantize.test_zero_tensor_and_amax_given]),
+    "block scale without the division by 6": (
+        [("float t = (a_b / 6.0f) * s_enc;", "float t = a_b * s_enc;")],
+        [lambda o: quantize.test_row_quantize_brute_force(o, "bf16", (32, 64))]),
+    "GEMM reads B transposed": (
+        [("acc += a[m * K + k] * b[n * K + k];", "acc += a[m * K + k] * b[k * N + n];")],
+        [lambda o: gemm.test_gemm_reduces_to_textbook_gemm(o, 8, 12, 16)]),
+}
+
+
+def _copy_oracle(dst, subs):
+    """The oracle package copied to dst with `subs` applied to its C source,
+    imported under a name of its own (it builds its own library in dst)."""
+    src = os.path.join(ROOT, "oracle")
+    os.makedirs(dst)
+    for f in ("__init__.py", "mlp.py", "nvfp4_oracle.c", "nvfp4_oracle.h"):
+        shutil.copy(os.path.join(src, f), os.path.join(dst, f))
+    c_path = os.path.join(dst, "nvfp4_oracle.c")
+    code = open(c_path).read()
+    for old, new in subs:
+        assert code.count(old) == 1, f"mutation site not unique: {old!r}"
+        code = code.replace(old, new)
+    open(c_path, "w").write(code)
+    name = "oracle_copy_" + os.path.basename(dst)
+    spec = importlib.util.spec_from_file_location(
+        name, os.path.join(dst, "__init__.py"), submodule_search_locations=[dst])
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod
+    spec.loader.exec_module(mod)
+    mod.build()
+    return mod
+
+
+def _pins_fail(orc, pins):
+    failed = []
+    for pin in pins:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError) as e:
+            failed.append((pin, e))
+    return failed
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    orc = _copy_oracle(str(tmp_path / "control"), [])
+    pins = [p for _, ps in MUTANTS.values() for p in ps]
+    assert not _pins_fail(orc, pins)
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    subs, pins = MUTANTS[name]
+    orc = _copy_oracle(str(tmp_path / "mutant"), subs)
+    assert _pins_fail(orc, pins), f"no pin noticed: {name}"
