@@ -7,6 +7,8 @@ three chained quantised operands gives relative errors of 0.2-0.3 at this
 size, while a swapped operand, a sign error or a permuted row gives errors
 above 1.
 """
+import importlib
+
 import numpy as np
 import pytest
 import torch
@@ -67,6 +69,12 @@ def test_swiglu_extreme_gates(orc):
     np.testing.assert_array_equal(_f64(got_dg[z:z + 3]), _f64(dh[z:z + 3]) * _f64(u[z:z + 3]) / 2)
 
 
+def _mlp(orc):
+    """The MLP composition of the oracle package `orc` (the oracle itself, or
+    a copy under test)."""
+    return importlib.import_module(orc.__name__ + ".mlp")
+
+
 def _torch_mlp(X, Wg, Wu, Wd, dY):
     Xt = torch.tensor(_f64(X), requires_grad=True)
     ws = [torch.tensor(w.astype(np.float64), requires_grad=True) for w in (Wg, Wu, Wd)]
@@ -83,7 +91,7 @@ def _rel(a, b):
 
 @pytest.mark.parametrize("rht", [False, True])
 def test_nvfp4_mlp_tracks_fp64_mlp(orc, rht):
-    from oracle.mlp import mlp_bwd, mlp_fwd
+    mlp_bwd, mlp_fwd = _mlp(orc).mlp_bwd, _mlp(orc).mlp_fwd
     M, D, F = 128, 64, 96
     X = syn.activations((M, D), seed=1)
     Wg = syn.weights((F, D), seed=4, master_fp32=True) * np.float32(5)
@@ -128,11 +136,10 @@ def _sr_decisions(orc, q, v_bits):
     return frac[keep], (mag == hi)[keep], keep
 
 
-def _rht_of_transpose(x_bits, seed):
+def _rht_of_transpose(orc, x_bits, seed):
     """(1/4) H16 diag(s) applied to each 16-element block of every row of x^T
     (x: bf16 bits [M, N] -> [N, M] float64), H16 = scipy's Sylvester matrix."""
     from scipy.linalg import hadamard
-    import oracle as orc
     xt = syn.bf16_bits_to_f32(x_bits).astype(np.float64).T
     T = hadamard(16) @ np.diag(orc.rht_signs(seed).astype(np.float64)) / 4.0
     n, m = xt.shape
@@ -141,7 +148,13 @@ def _rht_of_transpose(x_bits, seed):
 
 @pytest.fixture(scope="module")
 def mlp_run(orc):
-    from oracle.mlp import mlp_bwd, mlp_fwd
+    return make_mlp_run(orc)
+
+
+def make_mlp_run(orc):
+    """One forward and the backward of two steps of a small MLP, through the
+    composition of the oracle package `orc`."""
+    mlp_bwd, mlp_fwd = _mlp(orc).mlp_bwd, _mlp(orc).mlp_fwd
     M, D, F = 256, 64, 128
     X = syn.activations((M, D), seed=1)
     Wg = syn.weights((F, D), seed=4, master_fp32=True) * np.float32(5)
@@ -181,7 +194,7 @@ def test_mlp_sr_operands_draw_independent_words(orc, mlp_run):
     an offset would pair identical words, r < T1 and r < T2, a correlation of
     (min(f1, f2) - f1 f2) / sqrt(f1 (1 - f1) f2 (1 - f2)), about 0.5 here."""
     X, dY, saved, steps = mlp_run
-    from oracle.mlp import sr_offsets
+    sr_offsets = _mlp(orc).sr_offsets
     assert len(set(sr_offsets(0).values()) | set(sr_offsets(1).values())) == 12
     b0, b1 = steps
 
@@ -228,7 +241,7 @@ def test_mlp_wgrad_operands_carry_the_rht(orc, mlp_run):
                          ("dY^T", b["qdYc"], dY), ("dG^T", b["qdGc"], b["dG"]),
                          ("dU^T", b["qdUc"], b["dU"])):
         deq = orc.dequant(q)
-        T = _rht_of_transpose(src, 7)
+        T = _rht_of_transpose(orc, src, 7)
         plain = syn.bf16_bits_to_f32(src).astype(np.float64).T
         assert _rel(deq, T) < 0.3, (name, _rel(deq, T))
         assert _rel(deq, plain) > 0.7, (name, _rel(deq, plain))
@@ -239,7 +252,7 @@ def test_sgd_step_exact_on_representable_values(orc):
     """Integers times a power of two: every product and difference is exact in
     binary32, so the step must equal the exact FP64 result element for element,
     and the amax the largest magnitude of it."""
-    from oracle.mlp import sgd_step
+    sgd_step = _mlp(orc).sgd_step
     rng = np.random.Generator(np.random.PCG64(61))
     W = rng.integers(-4096, 4096, (48, 64)).astype(np.float32)
     G = rng.integers(-4096, 4096, (48, 64)).astype(np.float32)
@@ -257,7 +270,7 @@ def test_sgd_step_rounds_the_product_first(orc):
     W = 3 with G = 0.1 (not a binary32 value times lr = 0.1) checks the
     rounding of the difference against an FP64 evaluation of the same two
     rounded operations."""
-    from oracle.mlp import sgd_step
+    sgd_step = _mlp(orc).sgd_step
     one_ulp = np.float32(1 + 2.0 ** -23)
     W = np.array([[np.float32(1 + 2.0 ** -22), 3.0, -0.5, 7.0]], np.float32)
     G = np.array([[one_ulp, 0.1, 0.0, -2.0]], np.float32)
@@ -274,7 +287,7 @@ def test_sgd_step_zero_grad_and_zero_rate(orc):
     """zero_grad clears the gradient; lr = 0 leaves a weight without negative
     zeros unchanged bit for bit; the amax equals the one the oracle's 16x16
     quantiser takes of the updated weight (its own C reduction)."""
-    from oracle.mlp import sgd_step
+    sgd_step = _mlp(orc).sgd_step
     rng = np.random.Generator(np.random.PCG64(62))
     W = (rng.standard_normal((32, 48)) * 0.02).astype(np.float32)
     W[W == 0] = 1e-3

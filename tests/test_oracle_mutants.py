@@ -1,8 +1,9 @@
 """The oracle's pins catch plausible mistakes -- CPU only.
 
 Each case plants one mistake (a flipped tie rule, a wrong comparison, a
-dropped factor, a transposed index, a wrong constant) in a *copy* of the
-oracle's C source -- never in the oracle itself -- builds the copy as a
+dropped factor, a transposed index, a wrong constant, a wrong rounding mode
+or shared random stream in the MLP composition) in a *copy* of the oracle's
+source -- never in the oracle itself -- builds the copy as a
 separate package in a temporary directory and runs the pins that should
 notice it: at least one must fail.  The unmutated copy passes the same pins
 (the control), so a failure means the pin saw the mistake, not that the
@@ -10,6 +11,7 @@ copy is broken.  (Saturating E4M3 only from 480 is no such case: the
 encoder's final clamp to 0x7E gives the same codes.)
 """
 import importlib.util
+import itertools
 import os
 import shutil
 import sys
@@ -18,13 +20,16 @@ import pytest
 
 import test_oracle_formats as formats
 import test_oracle_gemm as gemm
+import test_oracle_mlp as mlp
 import test_oracle_philox as philox
 import test_oracle_quantize as quantize
 import test_oracle_rht as rht
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_COPIES = itertools.count()
 
-# name -> (substitutions in nvfp4_oracle.c, pins that must catch it)
+# name -> (substitutions (old, new) in nvfp4_oracle.c, or (file, old, new),
+#          pins that must catch it)
 MUTANTS = {
     "E2M1 ties away from zero": (
         [("else pick = ((lo & 1) == 0) ? lo : hi;", "else pick = hi;")],
@@ -68,6 +73,27 @@ MUTANTS = {
     "GEMM reads B transposed": (
         [("acc += a[m * K + k] * b[n * K + k];", "acc += a[m * K + k] * b[k * N + n];")],
         [lambda o: gemm.test_gemm_reduces_to_textbook_gemm(o, 8, 12, 16)]),
+    # the MLP composition (the recipe's per-operand choices)
+    "dG rounded to nearest instead of stochastically": (
+        [("mlp.py", 'qdG = quantize(dG, ROW_1X16, SR, seed=seed, offset=off["dg_row"])',
+          'qdG = quantize(dG, ROW_1X16, 0, seed=seed, offset=off["dg_row"])')],
+        [lambda o: mlp.test_mlp_gradient_operands_are_stochastically_rounded(
+            o, mlp.make_mlp_run(o))]),
+    "dU's row operand reuses dG's SR offset": (
+        [("mlp.py", '"du_row": b + 4', '"du_row": b + 2')],
+        [lambda o: mlp.test_mlp_sr_operands_draw_independent_words(o, mlp.make_mlp_run(o))]),
+    "H's WGRAD operand without the RHT": (
+        [("mlp.py", "qHc = quantize(H, COL_1X16, rf, seed=seed)",
+          "qHc = quantize(H, COL_1X16, 0, seed=seed)")],
+        [lambda o: mlp.test_mlp_wgrad_operands_carry_the_rht(o, mlp.make_mlp_run(o))]),
+    "dX without the up projection's term": (
+        [("mlp.py", "dX = bf16_round_f64(gemm_fp64(qdG, transposed_view(saved[\"qWg\"])) +\n"
+                    "                        gemm_fp64(qdU, transposed_view(saved[\"qWu\"])))",
+          "dX = bf16_round_f64(gemm_fp64(qdG, transposed_view(saved[\"qWg\"])))")],
+        [lambda o: mlp.test_nvfp4_mlp_tracks_fp64_mlp(o, True)]),
+    "SGD with the rate's sign flipped": (
+        [("mlp.py", "W_new = np.subtract(", "W_new = np.add(")],
+        [mlp.test_sgd_step_exact_on_representable_values]),
 }
 
 
@@ -78,13 +104,13 @@ def _copy_oracle(dst, subs):
     os.makedirs(dst)
     for f in ("__init__.py", "mlp.py", "nvfp4_oracle.c", "nvfp4_oracle.h"):
         shutil.copy(os.path.join(src, f), os.path.join(dst, f))
-    c_path = os.path.join(dst, "nvfp4_oracle.c")
-    code = open(c_path).read()
-    for old, new in subs:
+    for sub in subs:
+        fname, old, new = sub if len(sub) == 3 else ("nvfp4_oracle.c", *sub)
+        path = os.path.join(dst, fname)
+        code = open(path).read()
         assert code.count(old) == 1, f"mutation site not unique: {old!r}"
-        code = code.replace(old, new)
-    open(c_path, "w").write(code)
-    name = "oracle_copy_" + os.path.basename(dst)
+        open(path, "w").write(code.replace(old, new))
+    name = f"oracle_copy_{next(_COPIES)}"  # a fresh package (and mlp submodule) per copy
     spec = importlib.util.spec_from_file_location(
         name, os.path.join(dst, "__init__.py"), submodule_search_locations=[dst])
     mod = importlib.util.module_from_spec(spec)
