@@ -21,6 +21,7 @@ import pytest
 import test_oracle_formats as formats
 import test_oracle_gemm as gemm
 import test_oracle_mlp as mlp
+import test_oracle_mx as mx
 import test_oracle_philox as philox
 import test_oracle_quantize as quantize
 import test_oracle_rht as rht
@@ -73,6 +74,21 @@ MUTANTS = {
     "GEMM reads B transposed": (
         [("acc += a[m * K + k] * b[n * K + k];", "acc += a[m * K + k] * b[k * N + n];")],
         [lambda o: gemm.test_gemm_reduces_to_textbook_gemm(o, 8, 12, 16)]),
+    # the MX comparison formats
+    "E8M0 shared exponent offset 1 for E2M1": (
+        [("const int emax = fmt == ORC_MXFP8 ? 8 : 2;", "const int emax = fmt == ORC_MXFP8 ? 8 : 1;")],
+        [lambda o: mx.test_e8m0_scale_closed_forms(o, mx.MXFP4)]),
+    "MX elements scaled by twice the block scale": (
+        [("const float y = (float)ldexp((double)v[i], -((int)sb - 127));",
+          "const float y = (float)ldexp((double)v[i], -((int)sb - 126));")],
+        [lambda o: mx.test_elements_are_the_nearest_code(o, mx.MXFP4)]),
+    "MX column mode reads along rows": (
+        [("const int64_t idx = mode == ORC_MX_ROW ? r * ld + c : c * ld + r;",
+          "const int64_t idx = mode == ORC_MX_ROW ? r * ld + c : r * ld + c;")],
+        [lambda o: mx.test_column_mode_is_row_mode_of_transpose(o, mx.MXFP4)]),
+    "MX all-zero block drops the sign of zero": (
+        [("code = fmt == ORC_MXFP4 ? 0x8 : 0x80;  /* -0 in an all-zero block */", "code = 0;")],
+        [mx.test_zero_and_nonfinite_blocks]),
     # the MLP composition (the recipe's per-operand choices)
     "dG rounded to nearest instead of stochastically": (
         [("mlp.py", 'qdG = quantize(dG, ROW_1X16, SR, seed=seed, offset=off["dg_row"])',

@@ -9,23 +9,27 @@ import math
 import numpy as np
 import pytest
 
-import oracle as orc
 from nvfp4_block_scaled_03_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
-EMAX = {orc.MXFP4: 2, orc.MXFP8: 8}
+MXFP4, MXFP8 = 0, 1   # the oracle's format codes (checked below)
+EMAX = {MXFP4: 2, MXFP8: 8}
 
 
-def _values(fmt):
+def test_format_codes(orc):
+    assert (orc.MXFP4, orc.MXFP8) == (MXFP4, MXFP8)
+
+
+def _values(orc, fmt):
     """Decoded value of every element code (from the format tables)."""
     if fmt == orc.MXFP4:
         return np.array([orc.e2m1_value(c) for c in range(16)])
     return np.array([orc.e4m3_value(c) for c in range(256)])
 
 
-@pytest.mark.parametrize("fmt", [orc.MXFP4, orc.MXFP8])
-def test_e8m0_scale_closed_forms(fmt):
+@pytest.mark.parametrize("fmt", [MXFP4, MXFP8])
+def test_e8m0_scale_closed_forms(orc, fmt):
     e = EMAX[fmt]
     for k in range(-60, 61):
         p = math.ldexp(1.0, k)
@@ -42,7 +46,7 @@ def test_e8m0_scale_closed_forms(fmt):
     assert orc.e8m0_scale(float("nan"), fmt) == 0xFF
 
 
-def test_e8m0_values():
+def test_e8m0_values(orc):
     for b in range(255):
         assert orc.e8m0_value(b) == math.ldexp(1.0, b - 127)
     assert math.isnan(orc.e8m0_value(0xFF))
@@ -64,10 +68,10 @@ def _nearest_code(v, scale, vals):
     return best
 
 
-@pytest.mark.parametrize("fmt", [orc.MXFP4, orc.MXFP8])
-def test_elements_are_the_nearest_code(fmt):
+@pytest.mark.parametrize("fmt", [MXFP4, MXFP8])
+def test_elements_are_the_nearest_code(orc, fmt):
     rng = np.random.default_rng(11)
-    vals = _values(fmt)
+    vals = _values(orc, fmt)
     x = (rng.standard_normal((6, 64)) * np.exp(rng.uniform(-6, 6, (6, 1)))).astype(np.float32)
     x[0, :8] = [0.0, -0.0, 1e-30, -1e-30, 3.0, -3.0, 2.5, 5.0]  # zeros, tiny values, ties
     x[1, 5] = 0.0
@@ -87,10 +91,10 @@ def test_elements_are_the_nearest_code(fmt):
                 assert got == _nearest_code(v, scale, vals), (r, c, v)
 
 
-@pytest.mark.parametrize("fmt", [orc.MXFP4, orc.MXFP8])
-def test_representable_blocks_round_trip(fmt):
+@pytest.mark.parametrize("fmt", [MXFP4, MXFP8])
+def test_representable_blocks_round_trip(orc, fmt):
     rng = np.random.default_rng(5)
-    vals = _values(fmt)
+    vals = _values(orc, fmt)
     finite = vals[np.isfinite(vals)]
     top = np.max(np.abs(finite))
     for k in (-20, -3, 0, 7, 30):
@@ -101,8 +105,8 @@ def test_representable_blocks_round_trip(fmt):
         np.testing.assert_array_equal(orc.mx_dequant(q)[0], blk)
 
 
-@pytest.mark.parametrize("fmt", [orc.MXFP4, orc.MXFP8])
-def test_column_mode_is_row_mode_of_transpose(fmt):
+@pytest.mark.parametrize("fmt", [MXFP4, MXFP8])
+def test_column_mode_is_row_mode_of_transpose(orc, fmt):
     x = syn.activations((64, 96), seed=3)
     qc = orc.mx_quantize(x, orc.MX_COL, fmt)
     qr = orc.mx_quantize(np.ascontiguousarray(x.T), orc.MX_ROW, fmt)
@@ -110,7 +114,7 @@ def test_column_mode_is_row_mode_of_transpose(fmt):
     np.testing.assert_array_equal(qc["scales"], qr["scales"])
 
 
-def test_bf16_and_fp32_inputs_agree():
+def test_bf16_and_fp32_inputs_agree(orc):
     x = syn.activations((32, 128), seed=4)
     xf = orc.bf16_to_f32(x)
     for fmt in (orc.MXFP4, orc.MXFP8):
@@ -119,7 +123,7 @@ def test_bf16_and_fp32_inputs_agree():
         np.testing.assert_array_equal(a["scales"], b["scales"])
 
 
-def test_zero_and_nonfinite_blocks():
+def test_zero_and_nonfinite_blocks(orc):
     x = np.zeros((3, 32), np.float32)
     x[1, :] = -0.0
     x[2, 3] = np.inf
@@ -131,7 +135,7 @@ def test_zero_and_nonfinite_blocks():
         assert (q["codes"][1] == neg0).all()
 
 
-def test_nvfp4_error_below_mxfp4_on_outlier_data():
+def test_nvfp4_error_below_mxfp4_on_outlier_data(orc):
     """The page's comparison: 16-element blocks with E4M3 scales (under a
     per-tensor scale) encode the outlier-laden activations with less error
     than MXFP4's 32-element power-of-two blocks; MXFP8 (three mantissa bits)
