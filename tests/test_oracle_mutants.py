@@ -74,6 +74,21 @@ MUTANTS = {
     "GEMM reads B transposed": (
         [("acc += a[m * K + k] * b[n * K + k];", "acc += a[m * K + k] * b[k * N + n];")],
         [lambda o: gemm.test_gemm_reduces_to_textbook_gemm(o, 8, 12, 16)]),
+    "16x16 transposed scales taken from the wrong tile": (
+        [("out->scales_t[(tc * 16 + j) * (orows / 16) + tr] = sc;",
+          "out->scales_t[(tc * 16 + j) * (orows / 16) + (orows / 16 - 1 - tr)] = sc;")],
+        [quantize.test_16x16_one_scale_per_tile_and_transpose_invariant]),
+    "SR window ignores its index base": (
+        [("orc_sr_word(seed, offset, sr_index_base + (uint64_t)(r * ocols + c))",
+          "orc_sr_word(seed, offset, (uint64_t)(r * ocols + c))")],
+        [quantize.test_sr_window_equals_slab_of_whole]),
+    "BF16 rounding by truncation": (
+        [("double q = rint(ldexp(a, -lsb_exp));", "double q = floor(ldexp(a, -lsb_exp));")],
+        [formats.test_bf16_from_double_is_nearest_even]),
+    "SwiGLU with sigmoid(-g)": (
+        [("static double sigmoid_d(double g) { return 1.0 / (1.0 + exp(-g)); }",
+          "static double sigmoid_d(double g) { return 1.0 / (1.0 + exp(g)); }")],
+        [mlp.test_swiglu_matches_autograd]),
     # the MX comparison formats
     "E8M0 shared exponent offset 1 for E2M1": (
         [("const int emax = fmt == ORC_MXFP8 ? 8 : 2;", "const int emax = fmt == ORC_MXFP8 ? 8 : 1;")],
