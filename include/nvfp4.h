@@ -214,7 +214,7 @@ nvfp4_status nvfp4_quantize_rowcol(const void* x, int32_t in_dtype, int64_t rows
                                    nvfp4_tensor* row_out, nvfp4_tensor* col_out,
                                    nvfp4_stream stream);
 
-/* nvfp4_quantize without a workspace argument; the paper has no counterpart
+/* nvfp4_quantize without a workspace argument; the pages have no counterpart
  * to this entry point.  It is for callers that cannot provide device scratch
  * memory -- code running during CUDA graph capture (where cudaMalloc is not
  * allowed), plugins given only input and output pointers, or programs whose

@@ -1338,7 +1338,7 @@ int gemm_setup(GemmLaunchState& ls, K kern, uint32_t smem, int threads, int spli
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return 0;
       if (fa.numRegs * threads < split_regs) {
-        ls.resident[dev] = -1;  // this build can never run the kernel
+        ls.resident[dev] = -1;  // the compiled kernel can never run
         return 0;
       }
     }
