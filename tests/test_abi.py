@@ -273,3 +273,22 @@ def test_sgd_step_argument_errors_before_any_launch(lib):
     assert f(W, G, 64, 0.1, 0, A + 2, WS, 4096, None) == ALIGN
     assert f(W, G, 64, 0.1, 16, A, None, 0, None) == WORKSPACE
     assert f(W, G, 64, 0.1, 16, A, WS, 16, None) == WORKSPACE
+
+
+@pytest.mark.parametrize("std,cc", [("c11", "gcc"), ("c++17", "g++")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, std, cc):
+    """The boundary header stands alone: no CUDA or torch types, valid C11 and
+    C++17, warning-free, and every entry point has C linkage when included
+    from C++ (its names are not mangled)."""
+    import subprocess
+    ext = "c" if std == "c11" else "cpp"
+    src = tmp_path / f"use.{ext}"
+    init = "= {0}" if std == "c11" else "{}"
+    src.write_text('#include "nvfp4.h"\n'
+                   f"int probe(void) {{ nvfp4_tensor t {init}; (void)t;\n"
+                   "  return (int)nvfp4_quantize_sizes(128, 256, NVFP4_ROW_1X16, 0, 0, 0, 0, 0); }\n")
+    obj = tmp_path / "use.o"
+    subprocess.check_call([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-c",
+                           "-I", os.path.join(ROOT, "include"), str(src), "-o", str(obj)])
+    syms = subprocess.check_output(["nm", str(obj)], text=True)
+    assert re.search(r"\bU nvfp4_quantize_sizes\b", syms), syms
